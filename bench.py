@@ -1,0 +1,372 @@
+"""Throughput of the CacheGen codec on one GB300 per rank.
+
+One step = one pass of the whole hot path over the Llama-3-70B-shaped KV
+(L=80, H_kv=8, d=128, S=32768, fp16, 10.7 GB): cg_fit_tables (channel
+statistics, anchor scales, histograms, 16-bit CDFs), cg_encode (anchors,
+closed-loop deltas, rANS streams, size scan, compaction) and cg_decode
+(rANS decode + fused dequantisation into the KV layout).  Inputs are
+resident in HBM when the timed region starts and are larger than L2.
+
+The headline value is decode throughput (fp16 GB/s written by cg_decode);
+encode and fit throughput, the compression ratio, the entropy bound of the
+coded symbols, roofline fractions and an end-to-end figure through host
+buffers are reported beside it.  `--impl reference` times the CPU oracle on
+a bounded sample of the same workload instead.
+
+Multi-GPU: every rank codes its own copy of the workload (independent
+problems, no collective on the data path); value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode & encode GB/s of fp16 KV (70B shape, 1 GB300); ratio; % HBM roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_70b_L80_H8_d128_S32768")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.dev = dev
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel: str, per_launch_units: float):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (null otherwise)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            t = json.load(fh)[kernel]
+        src = open(os.path.join(ROOT, "kv_cache_compression_02_gb300", "csrc", t["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != t["source_sha"]:
+            return None
+        return t["dram_bytes_per_unit"] * per_launch_units
+    except Exception:
+        return None
+
+
+def generate_pinned(w, torch):
+    from kv_cache_compression_02_gb300 import synth
+    host = torch.empty(w.elements, dtype=torch.int16, pin_memory=True)
+    t0 = time.time()
+    synth.fill(w.gen, host.data_ptr())
+    return host, time.time() - t0
+
+
+def cpu_oracle_decode_rate(w, host_np, budget_s=10.0):
+    """Single-threaded oracle decode rate (fp16 bytes/s) on a bounded sample:
+    chunk-0 streams of successive heads, each fitted and encoded by the
+    oracle first (untimed), until budget_s of decode time has been spent."""
+    import oracle
+    oracle.build()
+    cd = oracle.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
+    L, H, S, d = w.L, w.H, w.S, w.d
+    spent, nbytes, streams = 0.0, 0, 0
+    heads = L * 2 * H
+    step_ = max(1, heads // 64)
+    for si in range(0, heads, step_):
+        l, kv, h = si // (2 * H), (si // H) % 2, si % H
+        head = host_np[si * S * d:(si + 1) * S * d].reshape(S, d)
+        m = [0.5, 1.0, 2.0][(3 * l) // L]
+        rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
+        n, blk, s, anc = oracle.encode_stream(cd, head, 0, st, rp, cdf)
+        out = np.zeros((S, d), np.uint16)
+        t0 = time.perf_counter()
+        rc = oracle.decode_stream(cd, blk, 0, st, cdf, s, anc, out)
+        spent += time.perf_counter() - t0
+        assert rc == 0
+        nbytes += min(w.C, S) * d * 2
+        streams += 1
+        if spent >= budget_s:
+            break
+    return nbytes / spent, spent, streams
+
+
+def run_reference(args):
+    """The CPU oracle on the machine's host cores (reference arm)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from kv_cache_compression_02_gb300 import synth, workloads as W
+    import oracle
+    w = W.BY_NAME[args.workload]
+    oracle.build()
+    # one bounded sample: 8 heads of the workload, their chunk-0 streams
+    heads = [(si // (2 * w.H), (si // w.H) % 2, si % w.H) for si in range(0, w.L * 2 * w.H, (w.L * 2 * w.H) // 8)][:8]
+    cd = oracle.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
+    prepared = []
+    for l, kv, h in heads:
+        head = synth.head(w.gen, l, kv, h)
+        m = [0.5, 1.0, 2.0][(3 * l) // w.L]
+        rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
+        n, blk, s, anc = oracle.encode_stream(cd, head, 0, st, rp, cdf)
+        prepared.append((blk, st, cdf, s, anc))
+    out = np.zeros((w.S, w.d), np.uint16)
+
+    def step():
+        for blk, st, cdf, s, anc in prepared:
+            assert oracle.decode_stream(cd, blk, 0, st, cdf, s, anc, out) == 0
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = len(prepared) * w.C * w.d * 2
+    v = nbytes / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+        "config": {"workload": w.name, "sample": f"chunk-0 streams of {len(prepared)} heads per step"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"decode of chunk 0 ({w.C} tokens x {w.d} lanes) of {len(prepared)} heads"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_compression_02_gb300 import build as cgbuild, cachegen as cg, workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cgbuild.build()
+    w = W.BY_NAME[args.workload]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    host, gen_s = generate_pinned(w, torch)
+    kv = host.to(dev, non_blocking=True)
+    cfg = cg.Config.from_workload(w)
+    tables = cg.empty_u8(cg.cg_tables_bytes(cfg))
+    ws_fit = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_FIT))
+    ws_enc = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_ENCODE))
+    ws_dec = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_DECODE))
+    out = cg.empty_u8(cg.cg_encode_bound(cfg))
+    nbytes_d = torch.zeros(1, dtype=torch.int64, device=dev)
+    kv_out = torch.empty_like(kv)
+    levels = w.levels_for()
+    torch.cuda.synchronize()
+
+    ev = {k: [] for k in ("fit", "enc", "dec")}
+    nbytes = None
+
+    def step(record: bool):
+        nonlocal nbytes
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        cg.check(cg.cg_fit_tables(cfg, kv, tables, ws_fit, stream), "cg_fit_tables")
+        e[1].record(stream)
+        cg.check(cg.cg_encode(cfg, tables, kv, levels, out, nbytes_d, ws_enc, stream), "cg_encode")
+        e[2].record(stream)
+        if nbytes is None:
+            torch.cuda.synchronize()
+            nbytes = int(nbytes_d.item())
+        cg.check(cg.cg_decode(cfg, tables, out, nbytes, 0, -1, kv_out, ws_dec, stream), "cg_decode")
+        e[3].record(stream)
+        if record:
+            ev["fit"].append((e[0], e[1]))
+            ev["enc"].append((e[1], e[2]))
+            ev["dec"].append((e[2], e[3]))
+
+    for _ in range(max(args.warmup, 1)):
+        step(False)
+    torch.cuda.synchronize()
+    for ws, what in ((ws_fit, "fit"), (ws_enc, "encode"), (ws_dec, "decode")):
+        cg.check(cg.cg_read_status(ws), what)
+    # sanity: the decode reproduces the input within the quantization error
+    xs = kv[: 1 << 20].float()
+    ys = kv_out[: 1 << 20].float()
+    if not torch.isfinite(ys).all() or (xs - ys).abs().max().item() > 0.5 * xs.abs().max().item():
+        raise RuntimeError("decoded KV does not match the input")
+
+    clocks = Clocks(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    ms = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    for ws, what in ((ws_fit, "fit"), (ws_enc, "encode"), (ws_dec, "decode")):
+        cg.check(cg.cg_read_status(ws), what)
+
+    # end to end through host buffers: container H2D, decode, KV D2H
+    cont_host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    cont_host.copy_(out[:nbytes])
+    out_host = torch.empty(kv.numel(), dtype=torch.int16, pin_memory=True)
+    cont_dev = cg.empty_u8(nbytes)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.e2e_steps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cont_dev.copy_(cont_host, non_blocking=True)
+        cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, 0, -1, kv_out, ws_dec, stream), "cg_decode")
+        out_host.copy_(kv_out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i:
+            e2e_ms.append(a.elapsed_time(b))
+    cg.check(cg.cg_read_status(ws_dec), "decode (e2e)")
+
+    # aggregate over ranks: max time, summed bytes
+    def agg_max(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms_dec, ms_enc, ms_fit = agg_max(ms["dec"]), agg_max(ms["enc"]), agg_max(ms["fit"])
+    ms_step_max = agg_max(ms_step)
+    ms_e2e = agg_max(statistics.mean(e2e_ms))
+    fp16 = w.fp16_bytes
+    dec_gbs = world * fp16 / (ms_dec * 1e-3) / 1e9
+    enc_gbs = world * fp16 / (ms_enc * 1e-3) / 1e9
+    fit_gbs = world * fp16 / (ms_fit * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    dec_alg = nbytes + fp16
+    enc_alg = fp16 + nbytes
+    dec_ach = dec_alg / (ms["dec"] * 1e-3) / 1e9
+    enc_ach = enc_alg / (ms["enc"] * 1e-3) / 1e9
+    tb_bytes = tables.numel()
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, spent, nstreams = cpu_oracle_decode_rate(w, host.numpy().view(np.uint16))
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"oracle decode of chunk-0 streams ({w.C} tokens x {w.d} lanes) of {nstreams} heads, "
+                         f"{spent:.1f} s"}
+    line = {
+        "metric": METRIC, "value": dec_gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32+f32", "data": "synthetic",
+        "config": {"workload": w.name, "L": w.L, "H_kv": w.H, "d": w.d, "S": w.S, "C": w.C, "G": w.G,
+                   "levels": list(w.level_base), "fp16_bytes": fp16, "l2": "inputs larger than L2 (10.7 GB)",
+                   "parallelism": f"independent replica per GPU x{world}"},
+        "decode_gbs": dec_gbs, "encode_gbs": enc_gbs, "fit_gbs": fit_gbs,
+        "ms": {"fit": ms_fit, "encode": ms_enc, "decode": ms_dec},
+        "ratio": fp16 / nbytes, "ratio_incl_tables": fp16 / (nbytes + tb_bytes),
+        "container_bytes": nbytes, "tables_bytes": tb_bytes,
+        "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": peak, "unit": "GB/s", "frac": dec_ach / peak,
+                     "traffic": traffic_for("k_decode", 1.0), "kernel": "cg_decode",
+                     "algorithmic_bytes_per_launch": dec_alg, "peak_kind": peak_kind,
+                     "frac_of_8TBs": dec_ach / 8000.0},
+        "roofline_encode": {"bound": "hbm", "achieved": enc_ach, "peak": peak, "unit": "GB/s",
+                            "frac": enc_ach / peak, "algorithmic_bytes_per_launch": enc_alg},
+        "e2e": {"value": world * fp16 / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": nbytes,
+                "d2h_bytes_per_step": fp16, "what": "pinned-host container -> cg_decode -> pinned-host KV"},
+        "gpu_launches": args.steps * (3 + 6 + 2),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "setup": {"generate_s": gen_s},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

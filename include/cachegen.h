@@ -1,0 +1,165 @@
+/*
+ * cachegen.h -- C ABI of libcachegen.so, a GB300 (sm_103a) implementation
+ * of the data-parallel hot path of the CacheGen KV-cache codec.
+ *
+ * What the codec computes (CacheGen, SIGCOMM'24, as the pages restate it):
+ *   - "Anchor-Based Delta Encoding" (Guide to CacheGen, pillar 2): tokens
+ *     are split into groups; the first token of each group is an anchor
+ *     kept at high precision (here int8 with a per-chunk, per-channel
+ *     absmax scale); the others are deltas against the anchor.
+ *   - "Layer Sensitivity Disparity" (Guide, pillar 1) and "layer-specific
+ *     compression levels" (gptget summary, Methodology): deltas are
+ *     quantized with a step b_level * m_layer * sigma_channel.
+ *   - "Distribution-Aware Arithmetic Coding" (Guide, pillar 3; gptget
+ *     Methodology, delta + arithmetic coding): quantized deltas are range
+ *     coded (rANS, 16-bit words, 2^16 total frequency) with one frequency
+ *     table per (level, layer, K/V, channel).
+ *   - Chunks with per-chunk compression levels, streamed and decoded in
+ *     step with transmission (gptget Methodology; Guide pillar 4
+ *     "Overlapped Streaming Decoder Pipeline").
+ *
+ * Conventions for every call:
+ *   - KV tensors are fp16, laid out [L][2][H][S][d] (layer, K=0/V=1, KV
+ *     head, token, head dim), contiguous, d innermost, 16-byte aligned.
+ *   - Pointers named *_dev are device pointers allocated by the caller;
+ *     the library allocates nothing and keeps no state between calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     compute calls are asynchronous on it; argument errors are returned
+ *     synchronously before anything is enqueued.
+ *   - Errors found on the device (non-finite input, a container or table
+ *     that fails validation, an output that does not fit) set bits of a
+ *     status word at the start of the caller's workspace; each call clears
+ *     it first.  Read it with cg_read_status() after synchronising.
+ *     Nothing traps or aborts; after an error the affected outputs are
+ *     unspecified, the CUDA context stays usable.
+ *   - GPU limits: 8 <= d <= 128 with d a multiple of 8; 1 <= G; 1 <= C;
+ *     1 <= S <= 2^22 (exact 128-bit channel moments); 1 <= n_levels <= 8; 0 <= alphabet_radius <= 127.
+ *
+ * Byte formats (little-endian, every section 16-byte aligned, padding 0):
+ *   tables:    64-byte header {"CGTB", u32 1, u32 L, H, d, n_levels, R, 0,
+ *              f32 level_base[8]}, f32 step[NL][L][2][H*d], f32
+ *              recip[NL][L][2][H*d], u16 cdf[NL][L][2][H*d][256].
+ *   container: 64-byte header {"CGKV", u32 1, u32 L, H, d, C, G, R, u64 S,
+ *              u32 n_levels, u32 n_chunks, u64 total_bytes, 0, 0},
+ *              u64 chunk_off[n_chunks]; per chunk k: {u16 level, u16 0,
+ *              u32 t0, u32 n_tok, u32 n_groups}, f32 s[L][2][H][d], i8
+ *              anchors[L][2][H][n_groups][d], u32 stream_off[L][2][H]
+ *              (from the chunk start), then one stream per (l, kv, h):
+ *              {u32 n_words, u32 n_esc, u32 n_delta, u32 0}, u32
+ *              state[d], u16 words[n_words] (decode order: token
+ *              ascending, lane ascending; per lane the renormalisation
+ *              word, then an escape's low and high halves).
+ */
+#ifndef CACHEGEN_H
+#define CACHEGEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CG_OK = 0,
+    CG_ERR_INVALID_ARG = 1, /* bad dims/params/pointer/size (synchronous)   */
+    CG_ERR_NONFINITE = 2,   /* an input element is Inf or NaN              */
+    CG_ERR_CAPACITY = 3,    /* output or workspace too small              */
+    CG_ERR_CORRUPT = 4,     /* container or tables failed validation      */
+    CG_ERR_CUDA = 5,        /* a CUDA launch or copy failed               */
+    CG_ERR_TIMEOUT = 6      /* reserved: no call waits on another agent   */
+} cg_status;
+
+typedef struct {
+    int32_t L;        /* layers                                          */
+    int32_t H;        /* KV heads per layer                              */
+    int32_t d;        /* head dim = rANS lanes per stream                */
+    int32_t C;        /* tokens per chunk (streaming / level unit)       */
+    int32_t G;        /* tokens per anchor group (first = anchor)        */
+    int32_t reserved; /* must be 0                                       */
+    int64_t S;        /* tokens                                          */
+} cg_dims;
+
+typedef struct {
+    int32_t n_levels;         /* compression levels, 1..8                  */
+    float level_base[8];      /* base step b_level (x sigma x multiplier)  */
+    const float *layer_mult;  /* host [L][2] multipliers (K, V); NULL =    */
+                              /* 0.5 / 1 / 2 for the first/middle/last     */
+                              /* third of the layers                       */
+    int32_t alphabet_radius;  /* R: |q| <= R coded directly, else escape   */
+} cg_params;
+
+enum { CG_OP_FIT = 0, CG_OP_ENCODE = 1, CG_OP_DECODE = 2 };
+
+/* Size in bytes of the tables blob for (dims, params).  0 on bad input. */
+size_t cg_tables_bytes(const cg_dims *dims, const cg_params *params);
+
+/* Workspace bytes needed by operation `op` (CG_OP_*).  0 on bad input.
+ * Encode needs about the fp16 size of the KV (word scratch); fit and
+ * decode need a few bytes per chunk and channel. */
+size_t cg_workspace_bytes(const cg_dims *dims, const cg_params *params, int op);
+
+/* Largest container cg_encode can produce for these dims: every stream
+ * holds at most one 16-bit word per delta symbol (escapes included; a
+ * stream that would need more is rejected with CG_ERR_CAPACITY), so this
+ * is about the fp16 size of the KV plus the anchors and headers.  An
+ * output buffer of this size only overflows together with that error. */
+cg_status cg_encode_bound(const cg_dims *dims, const cg_params *params, uint64_t *max_bytes);
+
+/* Fit the tables: per (layer, K/V, channel) sigma over all S tokens (exact
+ * integer moments, rounded once), step = max(b*m*sigma, 2^-12) and its
+ * reciprocal per level, and per (level, layer, K/V, channel) the 256-bin
+ * histogram of the delta symbols over all chunks, normalised to 16-bit
+ * frequencies (f_s = 1 + floor(n_s*65280/N), remainder to the most
+ * frequent symbol) and stored as CDFs.
+ *   kv_dev:     fp16 [L][2][H][S][d], read only.
+ *   tables_dev: cg_tables_bytes() bytes, written.
+ *   ws_dev:     cg_workspace_bytes(CG_OP_FIT) bytes, 256-byte aligned.
+ * Device errors: CG_ERR_NONFINITE. */
+cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void *kv_dev,
+                        void *tables_dev, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* Encode kv into a container (format above), chunk k at level
+ * chunk_level_host[k] (host array of n_chunks bytes, < n_levels).
+ *   out_dev:       out_capacity bytes; on success the first *out_bytes_dev
+ *                  bytes are the container (bit-identical to the oracle's).
+ *   out_bytes_dev: device u64, written with the container size (also when
+ *                  it exceeds out_capacity, so the caller can retry).
+ *   ws_dev:        cg_workspace_bytes(CG_OP_ENCODE) bytes.
+ * Device errors: CG_ERR_NONFINITE; CG_ERR_CAPACITY when the container does
+ * not fit in out_capacity (nothing past the header is written) or when one
+ * stream's words exceed its raw fp16 size (incompressible data). */
+cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                    const void *kv_dev, const uint8_t *chunk_level_host, void *out_dev,
+                    uint64_t out_capacity, uint64_t *out_bytes_dev, void *ws_dev,
+                    size_t ws_bytes, void *stream);
+
+/* Decode chunks [chunk_begin, chunk_end) of a container into the full KV
+ * buffer kv_dev (fp16 [L][2][H][S][d]; only those chunks' tokens are
+ * written).  chunk_end = -1 means all chunks.  dims/params must be the
+ * ones the container was made with (the kernel checks them against the
+ * container header).  The container must be bitstream_bytes long and the
+ * caller must keep it and the tables alive until the stream reaches the
+ * decode.  ws_dev: cg_workspace_bytes(CG_OP_DECODE) bytes.
+ * Device errors: CG_ERR_CORRUPT (header/offset/table mismatch, a stream
+ * whose lanes do not end in the initial state, or whose word or escape
+ * count disagrees with its header); decoding never reads outside the
+ * container. */
+cg_status cg_decode(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                    const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                    int32_t chunk_end, void *kv_dev, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* Status of the last call that used this workspace (blocking read of the
+ * device status word; synchronise the call's stream first). */
+cg_status cg_read_status(const void *ws_dev);
+
+/* Human-readable name of a status code (static string). */
+const char *cg_status_str(cg_status status);
+
+/* Library ABI version (1). */
+int32_t cg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,361 @@
+// cg_encode.cu -- the parallel range-coder encoder.
+//
+// CacheGen "encodes large tensors into compact bitstreams" with delta coding
+// plus arithmetic coding (gptget summary of arXiv 2310.07240, Methodology;
+// Guide to CacheGen, pillars 2-3).  Here every (chunk, layer, K/V, head) is
+// one rANS stream whose d lanes (channels) share one 16-bit word sequence.
+//
+//   k_encode          one CTA per (level, head); a team of d/4 threads
+//                     encodes one chunk's stream, 4 lanes per thread, in
+//                     reverse token order.  Per token the team orders its
+//                     words with a shuffle scan (lanes descending) and writes
+//                     them backwards into the stream's scratch slot, so the
+//                     scratch ends up in decode order.
+//   k_scan_chunks     per chunk: exclusive scan of the padded stream sizes.
+//   k_scan_total      chunk offsets and the container size.
+//   k_compact_fixed   container header, chunk headers, scales, anchors and
+//                     the stream index, copied into place.
+//   k_compact_stream  stream headers, states and words copied into place.
+// No kernel waits on another CTA; the scan is split into two launches.
+#include <cuda_fp16.h>
+
+#include "cg_kernels.cuh"
+
+namespace cg {
+namespace {
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// One rANS encode step after renormalisation (x < f * 2^16):
+//   x' = floor(x / f) * 2^16 + (x mod f) + cdf.
+// The quotient (< 2^16) is estimated in fp32 (relative error < 2^-21, so
+// the estimate is off by at most one) and corrected exactly.
+__device__ __forceinline__ uint32_t rans_put(uint32_t x, uint32_t f, uint32_t c) {
+  uint32_t q = __float2uint_rz(__fmul_rz(__uint2float_rz(x), rcp_approx(float(f))));
+  int32_t r = int32_t(x - q * f);
+  if (r < 0) {
+    q -= 1;
+    r += int32_t(f);
+  } else if (r >= int32_t(f)) {
+    q += 1;
+    r -= int32_t(f);
+  }
+  return (q << 16) + uint32_t(r) + c;
+}
+
+template <int T>
+__device__ __forceinline__ uint32_t team_mask() {
+  const int lane = threadIdx.x & 31;
+  return T == 32 ? 0xffffffffu : (((1u << T) - 1u) << (lane & ~(T - 1)));
+}
+
+constexpr int kLpt = kLanesPerThread;
+
+// ---------------------------------------------------------------- k_encode
+template <int T>
+__global__ void __launch_bounds__(kMaxTeams * T)
+k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv,
+         uint8_t *ws) {
+  extern __shared__ __align__(16) uint32_t etab[];  // [256][4][T] : cdf | f << 16
+  const int lv = blockIdx.x, si = blockIdx.y;
+  const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+  const int32_t *counts = reinterpret_cast<const int32_t *>(ws + w.levels);
+  const int32_t *lists = counts + kMaxLevels;
+  const int cnt = counts[lv];
+  if (cnt == 0) return;
+  uint32_t *status = reinterpret_cast<uint32_t *>(ws + w.status);
+
+  const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
+                        tab_index(lo, lv, l, kvi, h * lo.d) * 256;
+  for (int e = threadIdx.x; e < lo.d * 256; e += blockDim.x) {
+    const int c = e >> 8, s = e & 255;
+    const uint32_t c0 = cdf[c * 256 + s];
+    const uint32_t c1 = s < 255 ? cdf[c * 256 + s + 1] : kM;
+    etab[(s * kLpt + (c % kLpt)) * T + c / kLpt] = c0 | ((c1 - c0) << 16);
+  }
+  __syncthreads();
+
+  const int team = threadIdx.x / T, i = threadIdx.x % T, nteams = blockDim.x / T;
+  const uint32_t tm = team_mask<T>();
+  const float4 rc4 = *reinterpret_cast<const float4 *>(
+      reinterpret_cast<const float *>(tables + lo.tb_recip) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
+  const float rc[4] = {rc4.x, rc4.y, rc4.z, rc4.w};
+  const int R = lo.R;
+
+  for (int idx = team; idx < cnt; idx += nteams) {
+    const int k = lists[lv * lo.n_chunks + idx];
+    const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k);
+    const int64_t t0 = int64_t(k) * lo.C;
+    const uint8_t *chunk = ws + w.chunks + uint64_t(k) * lo.fixed_full;
+    const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
+    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
+    const uint16_t *xin = kv + (uint64_t(si) * lo.S + t0) * lo.d + kLpt * i;
+    const uint64_t sidx = uint64_t(k) * lo.nstr + si;
+    uint16_t *wout = reinterpret_cast<uint16_t *>(ws + w.words) + sidx * w.words_cap;
+    const int64_t cap = int64_t(w.words_cap);
+
+    uint32_t x[4] = {kRansL, kRansL, kRansL, kRansL};
+    int64_t E = 0;      // words emitted so far (encoder order)
+    uint32_t nesc = 0;
+    bool bad = false, overflow = false;
+    for (int g = ng - 1; g >= 0 && !overflow; g--) {
+      const uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
+      float ah[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
+      const int tend = min(g * lo.G + lo.G, ntok);
+      for (int tr = tend - 1; tr > g * lo.G; tr--) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tr) * lo.d));
+        const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+        uint32_t word[4], qv[4];
+        int nem[4];
+        bool esc[4], ren[4];
+        int cntw = 0;
+#pragma unroll
+        for (int j = 3; j >= 0; j--) {
+          if (((hw[j] >> 10) & 31u) == 31u) bad = true;
+          const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
+          const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
+          esc[j] = !(q >= -R && q <= R);
+          const int sym = esc[j] ? kEsc : q + 127;
+          const uint32_t e = etab[(sym * kLpt + j) * T + i];
+          const uint32_t f = e >> 16, c = e & 0xFFFFu;
+          ren[j] = x[j] >= (f << 16);
+          word[j] = x[j] & 0xFFFFu;
+          uint32_t xr = ren[j] ? (x[j] >> 16) : x[j];
+          x[j] = rans_put(xr, f, c);
+          qv[j] = uint32_t(q);
+          nem[j] = (esc[j] ? 2 : 0) + (ren[j] ? 1 : 0);
+          cntw += nem[j];
+        }
+        // emission order: lanes descending, i.e. threads descending
+        int suf = cntw;
+#pragma unroll
+        for (int o = 1; o < T; o <<= 1) {
+          const int v = __shfl_down_sync(tm, suf, o, T);
+          if (i + o < T) suf += v;
+        }
+        const int tot = __shfl_sync(tm, suf, 0, T);
+        if (E + tot > cap) {
+          overflow = true;
+          break;
+        }
+        int64_t e = E + (suf - cntw);
+#pragma unroll
+        for (int j = 3; j >= 0; j--) {
+          if (esc[j]) {
+            wout[cap - 1 - e] = uint16_t(qv[j] >> 16);
+            wout[cap - 2 - e] = uint16_t(qv[j] & 0xFFFFu);
+            e += 2;
+            nesc++;
+          }
+          if (ren[j]) {
+            wout[cap - 1 - e] = uint16_t(word[j]);
+            e += 1;
+          }
+        }
+        E += tot;
+      }
+    }
+    if (bad) atomicOr(status, kStNonfinite);
+    if (overflow) {
+      if (i == 0) atomicOr(status, kStCapacity);
+      continue;
+    }
+#pragma unroll
+    for (int o = T / 2; o; o >>= 1) nesc += __shfl_xor_sync(tm, nesc, o, T);
+    if (i == 0)
+      reinterpret_cast<uint2 *>(ws + w.info)[sidx] = make_uint2(uint32_t(E), nesc);
+    reinterpret_cast<uint4 *>(ws + w.states)[(sidx * lo.d) / 4 + i] = make_uint4(x[0], x[1], x[2], x[3]);
+  }
+}
+
+// ---------------------------------------------------------------- scans
+constexpr int kScanThreads = 1024;
+
+__device__ uint64_t block_excl_scan(uint64_t v, uint64_t *total, uint64_t *sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint64_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t s = lane < nw ? sm[lane] : 0;
+    uint64_t si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint64_t t = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += t;
+    }
+    sm[32 + lane] = si - s;
+    if (lane == 31) sm[64] = si;
+  }
+  __syncthreads();
+  const uint64_t r = sm[32 + warp] + incl - v;
+  *total = sm[64];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+k_scan_chunks(Layout lo, EncWs w, uint8_t *ws) {
+  __shared__ uint64_t sm[72];
+  const int k = blockIdx.x;
+  const uint2 *info = reinterpret_cast<const uint2 *>(ws + w.info) + uint64_t(k) * lo.nstr;
+  uint32_t *soff = reinterpret_cast<uint32_t *>(ws + w.soff) + uint64_t(k) * lo.nstr;
+  uint64_t rel = chunk_fixed(lo, k);
+  for (int base = 0; base < lo.nstr; base += kScanThreads) {
+    const int s = base + threadIdx.x;
+    const uint64_t sz = s < lo.nstr ? pad16(16 + 4 * uint64_t(lo.d) + 2 * uint64_t(info[s].x)) : 0;
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan(sz, &tot, sm);
+    if (s < lo.nstr) soff[s] = uint32_t(rel + ex);
+    rel += tot;
+  }
+  if (threadIdx.x == 0) reinterpret_cast<uint64_t *>(ws + w.coff)[k] = rel;  // chunk size for now
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+k_scan_total(Layout lo, EncWs w, uint8_t *ws, uint64_t cap, uint64_t *out_bytes) {
+  __shared__ uint64_t sm[72];
+  uint64_t *coff = reinterpret_cast<uint64_t *>(ws + w.coff);
+  uint64_t pos = lo.hdr_bytes;
+  for (int base = 0; base < lo.n_chunks; base += kScanThreads) {
+    const int k = base + threadIdx.x;
+    const uint64_t sz = k < lo.n_chunks ? coff[k] : 0;
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan(sz, &tot, sm);
+    if (k < lo.n_chunks) coff[k] = pos + ex;
+    pos += tot;
+  }
+  if (threadIdx.x == 0) {
+    coff[lo.n_chunks] = pos;
+    *out_bytes = pos;
+    if (pos > cap) atomicOr(reinterpret_cast<uint32_t *>(ws + w.status), kStCapacity);
+  }
+}
+
+// ---------------------------------------------------------------- compaction
+__global__ void __launch_bounds__(256)
+k_compact_fixed(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__restrict__ out) {
+  if (*reinterpret_cast<const uint32_t *>(ws + w.status) & (kStCapacity | kStNonfinite)) return;
+  const int k = blockIdx.x;
+  const uint64_t *coff = reinterpret_cast<const uint64_t *>(ws + w.coff);
+  const uint64_t base = coff[k];
+  const uint8_t *lv8 = ws + w.levels + 4 * kMaxLevels * (1 + uint64_t(lo.n_chunks));
+  if (k == 0) {
+    uint32_t *hd = reinterpret_cast<uint32_t *>(out);
+    for (uint64_t b = 64 + threadIdx.x * 8; b < lo.hdr_bytes; b += blockDim.x * 8) {
+      const uint64_t kk = (b - 64) / 8;
+      *reinterpret_cast<uint64_t *>(out + b) = kk < uint64_t(lo.n_chunks) ? coff[kk] : 0;
+    }
+    if (threadIdx.x == 0) {
+      hd[0] = 0x564B4743u;  // "CGKV"
+      hd[1] = 1;
+      hd[2] = lo.L;
+      hd[3] = lo.H;
+      hd[4] = lo.d;
+      hd[5] = lo.C;
+      hd[6] = lo.G;
+      hd[7] = lo.R;
+      *reinterpret_cast<uint64_t *>(out + 32) = uint64_t(lo.S);
+      hd[10] = lo.n_levels;
+      hd[11] = lo.n_chunks;
+      *reinterpret_cast<uint64_t *>(out + 48) = coff[lo.n_chunks];
+      hd[14] = 0;
+      hd[15] = 0;
+    }
+  }
+  uint32_t *dst = reinterpret_cast<uint32_t *>(out + base);
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(ws + w.chunks + uint64_t(k) * lo.fixed_full);
+  const uint32_t *soff = reinterpret_cast<const uint32_t *>(ws + w.soff) + uint64_t(k) * lo.nstr;
+  const uint64_t ng = chunk_ng(lo, k);
+  const uint64_t s_end = (lo.sec_s + 4 * uint64_t(lo.nstr) * lo.d) / 4;
+  const uint64_t a_beg = lo.sec_anc / 4, a_end = (lo.sec_anc + uint64_t(lo.nstr) * ng * lo.d) / 4;
+  const uint64_t o_beg = chunk_sec_off(lo, k) / 4, o_end = o_beg + lo.nstr;
+  const uint64_t nwords = chunk_fixed(lo, k) / 4;
+  for (uint64_t u = threadIdx.x; u < nwords; u += blockDim.x) {
+    uint32_t v = 0;
+    if (u == 0) v = lv8[k];
+    else if (u == 1) v = uint32_t(int64_t(k) * lo.C);
+    else if (u == 2) v = uint32_t(chunk_ntok(lo, k));
+    else if (u == 3) v = uint32_t(ng);
+    else if (u < s_end) v = src[u];
+    else if (u >= a_beg && u < a_end) v = src[u];
+    else if (u >= o_beg && u < o_end) v = soff[u - o_beg];
+    dst[u] = v;
+  }
+}
+
+__global__ void __launch_bounds__(128)
+k_compact_stream(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__restrict__ out) {
+  if (*reinterpret_cast<const uint32_t *>(ws + w.status) & (kStCapacity | kStNonfinite)) return;
+  const uint64_t ns = uint64_t(lo.n_chunks) * lo.nstr;
+  for (uint64_t sidx = blockIdx.x; sidx < ns; sidx += gridDim.x) {
+    const int k = int(sidx / lo.nstr);
+    const uint64_t base = reinterpret_cast<const uint64_t *>(ws + w.coff)[k] +
+                          reinterpret_cast<const uint32_t *>(ws + w.soff)[sidx];
+    const uint2 inf = reinterpret_cast<const uint2 *>(ws + w.info)[sidx];
+    uint8_t *blk = out + base;
+    if (threadIdx.x == 0)
+      *reinterpret_cast<uint4 *>(blk) = make_uint4(inf.x, inf.y, uint32_t(chunk_nd(lo, k)), 0u);
+    const uint32_t *st = reinterpret_cast<const uint32_t *>(ws + w.states) + sidx * lo.d;
+    uint32_t *sd = reinterpret_cast<uint32_t *>(blk + 16);
+    for (int j = threadIdx.x; j < lo.d; j += blockDim.x) sd[j] = st[j];
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(ws + w.words) + sidx * w.words_cap +
+                          (w.words_cap - inf.x);
+    uint16_t *wd = reinterpret_cast<uint16_t *>(blk + 16 + 4 * lo.d);
+    const uint64_t end = pad16(16 + 4 * uint64_t(lo.d) + 2 * uint64_t(inf.x));
+    const uint64_t nslots = (end - 16 - 4 * uint64_t(lo.d)) / 2;
+    for (uint64_t u = threadIdx.x; u < nslots; u += blockDim.x) wd[u] = u < inf.x ? src[u] : 0;
+  }
+}
+
+template <int T>
+cudaError_t launch_encode_t(const Layout &lo, const EncWs &w, const uint8_t *tables,
+                            const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
+  const size_t smem = size_t(256) * lo.d * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_encode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, lo.nstr);
+  k_encode<T><<<grid, teams * T, smem, st>>>(lo, w, tables, kv, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,
+                          const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
+  if (teams > kMaxTeams) teams = kMaxTeams;
+  if (teams < 1) return cudaSuccess;
+  switch (lo.d / kLpt) {
+    case 2: return launch_encode_t<2>(lo, w, tables, kv, ws, teams, st);
+    case 4: return launch_encode_t<4>(lo, w, tables, kv, ws, teams, st);
+    case 8: return launch_encode_t<8>(lo, w, tables, kv, ws, teams, st);
+    case 16: return launch_encode_t<16>(lo, w, tables, kv, ws, teams, st);
+    case 32: return launch_encode_t<32>(lo, w, tables, kv, ws, teams, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, uint8_t *out,
+                                uint64_t cap, uint64_t *out_bytes, cudaStream_t st) {
+  k_scan_chunks<<<lo.n_chunks, kScanThreads, 0, st>>>(lo, w, ws);
+  k_scan_total<<<1, kScanThreads, 0, st>>>(lo, w, ws, cap, out_bytes);
+  k_compact_fixed<<<lo.n_chunks, 256, 0, st>>>(lo, w, ws, out);
+  const uint64_t ns = uint64_t(lo.n_chunks) * lo.nstr;
+  const unsigned grid = unsigned(ns < 65536 ? ns : 65536);
+  k_compact_stream<<<grid, 128, 0, st>>>(lo, w, ws, out);
+  return cudaGetLastError();
+}
+
+}  // namespace cg

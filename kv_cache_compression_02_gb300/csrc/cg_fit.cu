@@ -1,0 +1,359 @@
+// cg_fit.cu -- fitting the per-(level, layer, K/V, channel) tables.
+//
+// The CacheGen pages build "empirical probability frequency tables for each
+// layer and head based on calibration profiling" (Guide to CacheGen, pillar
+// 3) and tune compression "by layer and channel sensitivity" (gptget
+// summary of arXiv 2310.07240, Methodology).  Three kernels:
+//   k_stats   sigma per channel from exact integer moments, then the step
+//             b*m*sigma (floored at 2^-12) and its reciprocal per level;
+//   k_anchor  per (chunk, head) the absmax of the anchor tokens -> scale s
+//             and 127/absmax (also used by the encoder, which additionally
+//             writes the int8 anchors);
+//   k_hist    per (level, head) the 256-bin histogram of the delta symbols
+//             over all chunks in shared memory, then the normalisation to
+//             16-bit frequencies and the CDF, one warp per channel.
+// All three are HBM-streaming kernels (no contraction, no tensor cores).
+#include <cuda_fp16.h>
+
+#include "cg_kernels.cuh"
+
+namespace cg {
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t half_bits(const uint4 &v, int i) {
+  uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
+  return uint16_t((i & 1) ? (w >> 16) : (w & 0xFFFF));
+}
+
+// fp16 value times 2^24 as an exact integer (|X| < 2^40)
+__device__ __forceinline__ int64_t f16_scaled(uint16_t h) {
+  uint32_t e = (h >> 10) & 31u;
+  uint64_t m = h & 1023u;
+  uint64_t v = e ? ((m | 1024u) << (e - 1)) : m;
+  return (h & 0x8000u) ? -int64_t(v) : int64_t(v);
+}
+
+// unsigned 128-bit integer to binary64, round to nearest even.  The top 64
+// bits (with the leading one at bit 63) carry the rounding; any nonzero bit
+// below them is folded into the lowest bit as a sticky bit, which lies
+// below the rounding position of a 53-bit significand.
+__device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
+  uint64_t hi = uint64_t(v >> 64);
+  if (hi == 0) return __ull2double_rn(uint64_t(v));
+  int sh = 64 - __clzll(hi);  // 1..64
+  uint64_t top = uint64_t(v >> sh);
+  uint64_t below = uint64_t(v) & ((sh == 64) ? ~0ull : ((1ull << sh) - 1));
+  top |= (below != 0) ? 1ull : 0ull;
+  return __dmul_rn(__ull2double_rn(top), __longlong_as_double(int64_t(1023 + sh) << 52));
+}
+
+// ---------------------------------------------------------------- k_stats
+// One CTA per head; each thread owns 8 channels (one 16-byte load per token)
+// and a strided subset of the tokens.  Integer sums are order-free, so the
+// reduction order does not matter for the result.
+constexpr int kStatsThreads = 256;
+
+__global__ void __launch_bounds__(kStatsThreads)
+k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables,
+        const float *__restrict__ mult, Bases bases, uint32_t *status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int si = blockIdx.x;
+  const int tpr = lo.d / 8;                 // threads per token row
+  const int rows = kStatsThreads / tpr;     // token rows in flight
+  const int col = threadIdx.x % tpr, row = threadIdx.x / tpr;
+  const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 8 * col;
+
+  int64_t T[8];
+  uint64_t Qlo[8], Qhi[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) { T[i] = 0; Qlo[i] = 0; Qhi[i] = 0; }
+  bool bad = false;
+  for (int64_t t = row; t < lo.S; t += rows) {
+    uint4 v = ld_nc_v4(head + t * lo.d);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      uint16_t h = half_bits(v, i);
+      if (((h >> 10) & 31u) == 31u) { bad = true; continue; }
+      int64_t X = f16_scaled(h);
+      T[i] += X;
+      uint64_t a = uint64_t(X < 0 ? -X : X);
+      uint64_t lo64 = a * a, hi64 = __umul64hi(a, a);
+      uint64_t s = Qlo[i] + lo64;
+      Qhi[i] += hi64 + (s < lo64 ? 1u : 0u);
+      Qlo[i] = s;
+    }
+  }
+  if (bad) atomicOr(status, kStNonfinite);
+
+  int64_t *sT = reinterpret_cast<int64_t *>(smem);          // [rows][d]
+  uint64_t *sQl = reinterpret_cast<uint64_t *>(sT + rows * lo.d);
+  uint64_t *sQh = sQl + rows * lo.d;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    int c = 8 * col + i;
+    sT[row * lo.d + c] = T[i];
+    sQl[row * lo.d + c] = Qlo[i];
+    sQh[row * lo.d + c] = Qhi[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < lo.d) {
+    const int c = threadIdx.x;
+    __int128 Ts = 0;
+    unsigned __int128 Qs = 0;
+    for (int r = 0; r < rows; r++) {
+      Ts += sT[r * lo.d + c];
+      Qs += (unsigned __int128)sQl[r * lo.d + c] | ((unsigned __int128)sQh[r * lo.d + c] << 64);
+    }
+    unsigned __int128 aT = (unsigned __int128)(Ts < 0 ? -Ts : Ts);
+    unsigned __int128 num = (unsigned __int128)(uint64_t)lo.S * Qs - aT * aT;
+    double var = __ddiv_rn(u128_to_double_rn(num),
+                           __ull2double_rn(uint64_t(lo.S) * uint64_t(lo.S)));
+    var = __dmul_rn(var, 0x1p-48);
+    float sigma = __double2float_rn(__dsqrt_rn(var));
+
+    const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+    const float m = mult[l * 2 + kvi];
+    float *stepv = reinterpret_cast<float *>(tables + lo.tb_step);
+    float *recipv = reinterpret_cast<float *>(tables + lo.tb_recip);
+    for (int lv = 0; lv < lo.n_levels; lv++) {
+      float st = __fmul_rn(__fmul_rn(bases.b[lv], m), sigma);
+      if (!(st >= 0x1p-12f)) st = 0x1p-12f;
+      uint64_t ix = tab_index(lo, lv, l, kvi, h * lo.d + c);
+      stepv[ix] = st;
+      recipv[ix] = __fdiv_rn(1.0f, st);
+    }
+  }
+  if (si == 0 && threadIdx.x == 0) {  // tables header
+    uint32_t *hd = reinterpret_cast<uint32_t *>(tables);
+    hd[0] = 0x42544743u;  // "CGTB"
+    hd[1] = 1;
+    hd[2] = lo.L;
+    hd[3] = lo.H;
+    hd[4] = lo.d;
+    hd[5] = lo.n_levels;
+    hd[6] = lo.R;
+    hd[7] = 0;
+    float *fb = reinterpret_cast<float *>(tables + 32);
+    for (int i = 0; i < kMaxLevels; i++) fb[i] = i < lo.n_levels ? bases.b[i] : 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------- k_anchor
+// One CTA per (chunk, head).  Fit mode writes (s, 127/absmax) per channel;
+// encode mode writes s and the int8 anchors into the chunk's fixed-part
+// scratch, laid out exactly as in the container.
+constexpr int kAnchorThreads = 256;
+
+__global__ void __launch_bounds__(kAnchorThreads)
+k_anchor(Layout lo, const uint16_t *__restrict__ kv, float2 *__restrict__ scale_out,
+         uint8_t *__restrict__ chunk_scratch, uint32_t *status) {
+  __shared__ float s_max[kAnchorThreads * 8];
+  __shared__ float s_inv[128];
+  const int k = blockIdx.x, si = blockIdx.y;
+  const int tpr = lo.d / 8, rows = kAnchorThreads / tpr;
+  const int col = threadIdx.x % tpr, row = threadIdx.x / tpr;
+  const int ng = chunk_ng(lo, k);
+  const int64_t t0 = int64_t(k) * lo.C;
+  const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 8 * col;
+
+  float amax[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) amax[i] = 0.0f;
+  bool bad = false;
+  for (int g = row; g < ng; g += rows) {
+    uint4 v = ld_nc_v4(head + (t0 + int64_t(g) * lo.G) * lo.d);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      uint16_t h = half_bits(v, i);
+      if (((h >> 10) & 31u) == 31u) { bad = true; continue; }
+      amax[i] = fmaxf(amax[i], fabsf(__half2float(__ushort_as_half(h))));
+    }
+  }
+  if (bad) atomicOr(status, kStNonfinite);
+#pragma unroll
+  for (int i = 0; i < 8; i++) s_max[row * lo.d + 8 * col + i] = amax[i];
+  __syncthreads();
+  if (threadIdx.x < lo.d) {
+    const int c = threadIdx.x;
+    float a = 0.0f;
+    for (int r = 0; r < rows; r++) a = fmaxf(a, s_max[r * lo.d + c]);
+    float s = 0.0f, inv = 0.0f;
+    if (a != 0.0f) {
+      s = __fdiv_rn(a, 127.0f);
+      inv = __fdiv_rn(127.0f, a);
+    }
+    if (scale_out) scale_out[(uint64_t(k) * lo.nstr + si) * lo.d + c] = make_float2(s, inv);
+    s_inv[c] = inv;
+    if (chunk_scratch) {
+      float *sv = reinterpret_cast<float *>(chunk_scratch + uint64_t(k) * lo.fixed_full + lo.sec_s);
+      sv[uint64_t(si) * lo.d + c] = s;
+    }
+  }
+  if (!chunk_scratch) return;
+  __syncthreads();
+  int8_t *anc = reinterpret_cast<int8_t *>(chunk_scratch + uint64_t(k) * lo.fixed_full + lo.sec_anc);
+  for (int g = row; g < ng; g += rows) {
+    uint4 v = ld_nc_v4(head + (t0 + int64_t(g) * lo.G) * lo.d);
+    uint32_t packed[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      float x = __half2float(__ushort_as_half(half_bits(v, i)));
+      int a = __float2int_rn(__fmul_rn(x, s_inv[8 * col + i]));
+      a = max(-127, min(127, a));
+      packed[i / 4] |= (uint32_t(a) & 0xFFu) << (8 * (i % 4));
+    }
+    *reinterpret_cast<uint2 *>(anc + (uint64_t(si) * ng + g) * lo.d + 8 * col) =
+        make_uint2(packed[0], packed[1]);
+  }
+}
+
+// ---------------------------------------------------------------- k_hist
+// One CTA per (level, head).  Threads work on channel pairs; a team of d/2
+// threads takes one anchor group at a time: it rebuilds a_hat from the
+// chunk's scale, quantizes the group's deltas and counts the symbols into
+// a shared [d][257] histogram (the odd row stride spreads channels over
+// banks).  Then one warp per channel normalises its counts.
+constexpr int kHistThreads = 512;
+
+__global__ void __launch_bounds__(kHistThreads)
+k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ scale,
+       uint8_t *__restrict__ tables) {
+  extern __shared__ __align__(16) uint32_t hist[];  // [d][257]
+  const int lv = blockIdx.x, si = blockIdx.y;
+  const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+  for (int i = threadIdx.x; i < lo.d * 257; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+
+  const int tpr = lo.d / 2, teams = kHistThreads / tpr;
+  const int col = threadIdx.x % tpr, team = threadIdx.x / tpr;
+  const int c0 = 2 * col;
+  const float *recipv = reinterpret_cast<const float *>(tables + lo.tb_recip);
+  const uint64_t ti = tab_index(lo, lv, l, kvi, h * lo.d + c0);
+  const float r0 = recipv[ti], r1 = recipv[ti + 1];
+  const uint32_t *head = reinterpret_cast<const uint32_t *>(kv + uint64_t(si) * lo.S * lo.d + c0);
+  const int dw = lo.d / 2;  // u32 words per token row
+  const int64_t n_groups = int64_t(lo.n_chunks - 1) * lo.ng_full + lo.ng_last;
+  const int R = lo.R;
+
+  for (int64_t gi = team; gi < n_groups; gi += teams) {
+    const int k = int(gi / lo.ng_full), g = int(gi % lo.ng_full);
+    const int64_t t0 = int64_t(k) * lo.C;
+    const int64_t ta = t0 + int64_t(g) * lo.G;
+    const int64_t te = min(ta + lo.G, t0 + chunk_ntok(lo, k));
+    const float2 sc0 = scale[(uint64_t(k) * lo.nstr + si) * lo.d + c0];
+    const float2 sc1 = scale[(uint64_t(k) * lo.nstr + si) * lo.d + c0 + 1];
+    uint32_t wa = __ldg(head + ta * dw);
+    float xa0 = __half2float(__ushort_as_half(uint16_t(wa & 0xFFFF)));
+    float xa1 = __half2float(__ushort_as_half(uint16_t(wa >> 16)));
+    int a0 = max(-127, min(127, __float2int_rn(__fmul_rn(xa0, sc0.y))));
+    int a1 = max(-127, min(127, __float2int_rn(__fmul_rn(xa1, sc1.y))));
+    const float ah0 = __fmul_rn(float(a0), sc0.x), ah1 = __fmul_rn(float(a1), sc1.x);
+    for (int64_t t = ta + 1; t < te; t++) {
+      uint32_t w = __ldg(head + t * dw);
+      float x0 = __half2float(__ushort_as_half(uint16_t(w & 0xFFFF)));
+      float x1 = __half2float(__ushort_as_half(uint16_t(w >> 16)));
+      int q0 = __float2int_rn(__fmul_rn(__fsub_rn(x0, ah0), r0));
+      int q1 = __float2int_rn(__fmul_rn(__fsub_rn(x1, ah1), r1));
+      int s0 = (q0 >= -R && q0 <= R) ? q0 + 127 : kEsc;
+      int s1 = (q1 >= -R && q1 <= R) ? q1 + 127 : kEsc;
+      atomicAdd(&hist[c0 * 257 + s0], 1u);
+      atomicAdd(&hist[(c0 + 1) * 257 + s1], 1u);
+    }
+  }
+  __syncthreads();
+
+  // normalisation: one warp per channel, 8 symbols per lane
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  uint16_t *cdfv = reinterpret_cast<uint16_t *>(tables + lo.tb_cdf);
+  for (int c = warp; c < lo.d; c += nwarps) {
+    uint32_t n[8];
+    uint32_t nsum = 0, best = 0;
+    int bests = 8 * lane;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      n[i] = hist[c * 257 + 8 * lane + i];
+      nsum += n[i];
+      if (n[i] > best) { best = n[i]; bests = 8 * lane + i; }
+    }
+    uint32_t N = nsum;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) N += __shfl_xor_sync(0xffffffffu, N, o);
+    // argmax with the lowest symbol on ties
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      uint32_t ob = __shfl_xor_sync(0xffffffffu, best, o);
+      int os = __shfl_xor_sync(0xffffffffu, bests, o);
+      if (ob > best || (ob == best && os < bests)) { best = ob; bests = os; }
+    }
+    const int arg = N ? bests : 127;
+    uint32_t f[8], fsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      f[i] = 1u + (N ? uint32_t((uint64_t(n[i]) * (kM - 256u)) / N) : 0u);
+      fsum += f[i];
+    }
+    uint32_t F = fsum;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) F += __shfl_xor_sync(0xffffffffu, F, o);
+    if (arg >= 8 * lane && arg < 8 * lane + 8) {
+      f[arg - 8 * lane] += kM - F;
+      fsum += kM - F;
+    }
+    uint32_t incl = fsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    uint32_t run = incl - fsum;
+    uint32_t packed[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      uint32_t c_a = run;
+      run += f[i];
+      uint32_t c_b = run;
+      run += f[i + 1];
+      packed[i / 2] = (c_a & 0xFFFFu) | (c_b << 16);
+    }
+    uint64_t ix = tab_index(lo, lv, l, kvi, h * lo.d + c);
+    *reinterpret_cast<uint4 *>(cdfv + ix * 256 + 8 * lane) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
+                         Bases bases, uint32_t *status, cudaStream_t st) {
+  const int rows = kStatsThreads / (lo.d / 8);
+  const size_t smem = size_t(rows) * lo.d * 24;
+  k_stats<<<lo.nstr, kStatsThreads, smem, st>>>(lo, kv, tables, mult, bases, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *scale_out,
+                                 uint8_t *chunk_scratch, uint32_t *status, cudaStream_t st) {
+  dim3 grid(lo.n_chunks, lo.nstr);
+  k_anchor<<<grid, kAnchorThreads, 0, st>>>(lo, kv, scale_out, chunk_scratch, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
+                        uint8_t *tables, cudaStream_t st) {
+  const size_t smem = size_t(lo.d) * 257 * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, lo.nstr);
+  k_hist<<<grid, kHistThreads, smem, st>>>(lo, kv, scale, tables);
+  return cudaGetLastError();
+}
+
+}  // namespace cg

@@ -1,0 +1,34 @@
+// cg_kernels.cuh -- host-side launchers of the codec's kernels (one per
+// translation unit), called by the C-ABI entry points in cg_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "cg_layout.cuh"
+
+namespace cg {
+
+struct Bases {
+  float b[kMaxLevels];
+};
+
+// cg_fit.cu
+cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
+                         Bases bases, uint32_t *status, cudaStream_t st);
+cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *scale_out,
+                                 uint8_t *chunk_scratch, uint32_t *status, cudaStream_t st);
+cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
+                        uint8_t *tables, cudaStream_t st);
+
+// cg_encode.cu
+cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,
+                          const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st);
+cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, uint8_t *out,
+                                uint64_t cap, uint64_t *out_bytes, cudaStream_t st);
+
+// cg_decode.cu
+cudaError_t launch_decode(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
+                          uint64_t bytes, int32_t k0, int32_t k1, uint16_t *kv, uint8_t *ws,
+                          cudaStream_t st);
+
+}  // namespace cg

@@ -388,7 +388,7 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static int dims_ok(const orc_dims *dm)
 {
     return dm->L >= 1 && dm->H >= 1 && dm->d >= 1 && dm->C >= 1 && dm->G >= 1 &&
-           dm->S >= 1 && dm->R >= 0 && dm->R <= 127;
+           dm->S >= 1 && dm->S <= ((int64_t)1 << 22) && dm->R >= 0 && dm->R <= 127;
 }
 
 size_t orc_tables_bytes(const orc_dims *dm, int32_t n_levels)

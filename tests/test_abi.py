@@ -1,0 +1,83 @@
+"""The C ABI: the library loads, exports every function include/cachegen.h
+declares, and its host-only size queries agree with the oracle (no GPU)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from kv_cache_compression_02_gb300 import build, cachegen as cg
+from kv_cache_compression_02_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return cg.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(cg_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert cg.cg_version() == 1
+    assert cg.cg_status_str(cg.CG_ERR_CORRUPT) == "CG_ERR_CORRUPT"
+    assert cg.cg_status_str(99) == "CG_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("w", [W.TINY, W.LLAMA7B, W.LLAMA3_8B, W.LLAMA3_70B, W.LONGCTX_MIXED], ids=lambda w: w.name)
+def test_sizes_match_oracle(orc, lib, w):
+    cfg = cg.Config.from_workload(w)
+    cd = orc.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
+    assert cg.cg_tables_bytes(cfg) == orc.tables_bytes(cd, w.n_levels)
+    # one word slot per delta symbol per stream, plus the fixed parts
+    nk, nstr = w.n_chunks, w.L * 2 * w.H
+    pad = lambda v: (v + 15) // 16 * 16  # noqa: E731
+    bound = pad(64 + 8 * nk)
+    for k in range(nk):
+        ntok = min(w.C, w.S - k * w.C)
+        ng = -(-ntok // w.G)
+        bound += 16 + pad(4 * nstr * w.d) + pad(nstr * ng * w.d) + pad(4 * nstr)
+        bound += nstr * pad(16 + 4 * w.d + 2 * (ntok - ng) * w.d)
+    assert cg.cg_encode_bound(cfg) == bound
+    for op in (cg.CG_OP_FIT, cg.CG_OP_ENCODE, cg.CG_OP_DECODE):
+        assert cg.cg_workspace_bytes(cfg, op) > 0
+
+
+def test_invalid_arguments(lib):
+    bad = [dict(L=1, H=1, d=12, S=10, C=10), dict(L=1, H=1, d=256, S=10, C=10), dict(L=1, H=1, d=8, S=0, C=10),
+           dict(L=1, H=1, d=8, S=10, C=0), dict(L=1, H=1, d=8, S=10, C=10, G=0),
+           dict(L=1, H=1, d=8, S=10, C=10, R=128), dict(L=1, H=1, d=8, S=2 ** 22 + 1, C=10),
+           dict(L=1, H=1, d=8, S=10, C=10, level_base=()), dict(L=1, H=1, d=8, S=10, C=10, level_base=(0.1,) * 9),
+           dict(L=1, H=1, d=8, S=10, C=10, level_base=(float("nan"),)),
+           dict(L=1, H=1, d=8, S=10, C=10, layer_mult=np.array([[1.0, -1.0]]))]
+    for kw in bad:
+        lb = kw.pop("level_base", (0.1,))
+        if len(lb) > 8:
+            continue  # cannot even be expressed in cg_params
+        cfg = cg.Config(level_base=lb, **kw)
+        if len(lb) == 0:
+            cfg.params.n_levels = 0
+        assert cg.cg_tables_bytes(cfg) == 0, kw
+        assert cg.cg_workspace_bytes(cfg, cg.CG_OP_DECODE) == 0, kw
+        with pytest.raises(cg.CacheGenError):
+            cg.cg_encode_bound(cfg)
+    cfg = cg.Config(L=1, H=1, d=8, S=10, C=10)
+    assert cg.cg_workspace_bytes(cfg, 7) == 0
+    assert lib.cg_fit_tables(None, None, None, None, None, 0, None) == cg.CG_ERR_INVALID_ARG
