@@ -99,11 +99,14 @@ size_t cg_tables_bytes(const cg_dims *dims, const cg_params *params);
  * decode need a few bytes per chunk and channel. */
 size_t cg_workspace_bytes(const cg_dims *dims, const cg_params *params, int op);
 
-/* Largest container cg_encode can produce for these dims: every stream
- * holds at most one 16-bit word per delta symbol (escapes included; a
- * stream that would need more is rejected with CG_ERR_CAPACITY), so this
- * is about the fp16 size of the KV plus the anchors and headers.  An
- * output buffer of this size only overflows together with that error. */
+/* Largest container cg_encode can produce for these dims.  With the full
+ * alphabet (alphabet_radius 127) every stream holds at most one 16-bit word
+ * per delta symbol, escapes included: a stream that would need more (more
+ * than its raw fp16 size) is rejected with CG_ERR_CAPACITY.  So the bound
+ * is about the fp16 size of the KV plus anchors and headers.  With a
+ * smaller radius, where most symbols may escape, the limit is three words
+ * per symbol.  An output of this size only overflows along with that
+ * error. */
 cg_status cg_encode_bound(const cg_dims *dims, const cg_params *params, uint64_t *max_bytes);
 
 /* Fit the tables: per (layer, K/V, channel) sigma over all S tokens (exact
@@ -127,8 +130,8 @@ cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void
  *                  it exceeds out_capacity, so the caller can retry).
  *   ws_dev:        cg_workspace_bytes(CG_OP_ENCODE) bytes.
  * Device errors: CG_ERR_NONFINITE; CG_ERR_CAPACITY when the container does
- * not fit in out_capacity (nothing past the header is written) or when one
- * stream's words exceed its raw fp16 size (incompressible data). */
+ * not fit in out_capacity (nothing is written) or when one stream's words
+ * exceed the per-symbol limit described at cg_encode_bound. */
 cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *tables_dev,
                     const void *kv_dev, const uint8_t *chunk_level_host, void *out_dev,
                     uint64_t out_capacity, uint64_t *out_bytes_dev, void *ws_dev,

@@ -71,7 +71,8 @@ cg_status cg_encode_bound(const cg_dims *dims, const cg_params *params, uint64_t
   uint64_t total = lo.hdr_bytes;
   for (int64_t k = 0; k < lo.n_chunks; k++)
     total += chunk_fixed(lo, k) +
-             uint64_t(lo.nstr) * pad16(16 + 4 * uint64_t(lo.d) + 2 * uint64_t(chunk_nd(lo, k)) * lo.d);
+             uint64_t(lo.nstr) * pad16(16 + 4 * uint64_t(lo.d) +
+                                       2 * words_per_symbol(lo) * uint64_t(chunk_nd(lo, k)) * lo.d);
   *max_bytes = total;
   return CG_OK;
 }

@@ -96,6 +96,12 @@ inline bool make_layout(Layout &lo, int32_t L, int32_t H, int32_t d, int32_t C, 
   return true;
 }
 
+// Word slots a stream may use per delta symbol.  With the full alphabet
+// (R = 127) escapes are rare and a stream that needs more than one 16-bit
+// word per symbol expands its raw fp16 size, which the encoder rejects;
+// with a smaller alphabet most symbols may escape (3 words each).
+__host__ __device__ inline uint64_t words_per_symbol(const Layout &lo) { return lo.R < 127 ? 3 : 1; }
+
 // ---- workspaces ----------------------------------------------------------
 // Every workspace starts with a 256-byte status block.
 struct FitWs {
@@ -126,7 +132,7 @@ inline EncWs enc_ws(const Layout &lo) {
   w.states = pad256(w.info + 8 * ns);                              // u32 [ns][d]
   w.soff = pad256(w.states + 4 * ns * lo.d);                       // u32 [ns]
   w.coff = pad256(w.soff + 4 * ns);                                // u64 [nk] + total
-  w.words_cap = uint64_t(lo.nd_full) * lo.d;
+  w.words_cap = uint64_t(lo.nd_full) * lo.d * words_per_symbol(lo);
   w.words = pad256(w.coff + 8 * (uint64_t(lo.n_chunks) + 1));      // u16 [ns][cap]
   w.bytes = pad256(w.words + 2 * ns * w.words_cap);
   return w;
