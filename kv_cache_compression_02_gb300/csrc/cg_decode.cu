@@ -36,10 +36,13 @@ constexpr int kLpt = kLanesPerThread;
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 __device__ __forceinline__ uint64_t ld_u64(const uint8_t *p) { return *reinterpret_cast<const uint64_t *>(p); }
 
-__device__ __forceinline__ uint16_t ld_word(const uint16_t *p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
+// Two fp32 values to packed fp16 (lo in the low half), round to nearest
+// even, saturating to +-65504 instead of overflowing to infinity: the same
+// result as clamping to the finite fp16 range and then rounding.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // ---------------------------------------------------------------- index
@@ -98,12 +101,13 @@ __device__ __forceinline__ uint32_t team_mask() {
 // Thread i of a team owns lanes 4i..4i+3; its entries sit at word index
 // (row * T + i), so with T = 32 every access of thread i hits bank i.
 template <int T>
-__global__ void __launch_bounds__(kMaxTeams * T)
+__global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws) {
   extern __shared__ __align__(16) uint32_t smem[];
   uint32_t *etab = smem;
   uint8_t *lut = reinterpret_cast<uint8_t *>(smem + 257 * kLpt * T);
+  uint16_t *crow = reinterpret_cast<uint16_t *>(lut + 256 * kLpt * T);  // [d][256] cdf, row layout
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
@@ -125,6 +129,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     if (c1 <= c0 || (s == 0 && c0 != 0)) s_bad = 1;
     const int j = c % kLpt, ti = c / kLpt;
     etab[(s * kLpt + j) * T + ti] = c0 | ((c1 - c0) << 16);
+    crow[c * 256 + s] = uint16_t(c0);
     if (s == 0) etab[(256 * kLpt + j) * T + ti] = 0;
     for (uint32_t b = (c0 + 255) >> 8; b <= ((c1 - 1) >> 8) && c1 > c0; b++)
       lut[(b * T + ti) * kLpt + j] = uint8_t(s);
@@ -171,7 +176,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     }
     const uint4 xs = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * i);
     uint32_t x[4] = {xs.x, xs.y, xs.z, xs.w};
-    const uint16_t *words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
+    const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
     const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
     const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
@@ -179,43 +184,71 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     uint32_t p = 0, nesc = 0;
     bool broken = false;
 
+    uint16_t *orow = out;
     for (int g = 0; g < ng && !broken; g++) {
       const uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
       float ah[4];
 #pragma unroll
       for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
-      {
-        __half2 h01 = __floats2half2_rn(ah[0], ah[1]);
-        __half2 h23 = __floats2half2_rn(ah[2], ah[3]);
-        *reinterpret_cast<uint2 *>(out + uint64_t(g) * lo.G * lo.d) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
-      }
-      const int tend = min(g * lo.G + lo.G, ntok);
-      for (int tr = g * lo.G + 1; tr < tend; tr++) {
-        uint32_t sym[4], need[4];
-        int cntw = 0;
+      *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(ah[0], ah[1]), pack_f16x2(ah[2], ah[3]));
+      orow += lo.d;
+      const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
+      for (int tt = 0; tt < nt; tt++, orow += lo.d) {
+        // ---- symbol search: bucket LUT, then at most one step forward
+        uint32_t sy[4], ee[4], rr[4];
+        uint32_t slow = 0;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           const uint32_t slot = x[j] & 0xFFFFu;
-          uint32_t s = lt[(slot >> 8) * (T * kLpt) + j];
-          uint32_t e = et[(s * kLpt + j) * T];
-          const uint32_t e1 = et[((s + 1) * kLpt + j) * T];
-          uint32_t r = slot - (e & 0xFFFFu);
-          if (r >= (e >> 16)) {
-            r -= e >> 16;
-            s += 1;
-            e = e1;
-            while (r >= (e >> 16) && s < 255) {  // bucket holding 3+ symbols
-              r -= e >> 16;
-              s += 1;
-              e = et[(s * kLpt + j) * T];
+          const uint32_t s0 = lt[((x[j] >> 8) & 0xFFu) * (T * kLpt) + j];  // bucket = slot >> 8
+          const uint32_t e0 = et[(s0 * kLpt + j) * T];
+          const uint32_t e1 = et[((s0 + 1) * kLpt + j) * T];
+          const uint32_t r0 = slot - (e0 & 0xFFFFu);
+          const uint32_t f0 = e0 >> 16;
+          const bool p = r0 >= f0;
+          rr[j] = p ? r0 - f0 : r0;
+          ee[j] = p ? e1 : e0;
+          sy[j] = s0 + (p ? 1u : 0u);
+          slow |= (p && rr[j] >= (e1 >> 16)) ? (1u << j) : 0u;
+        }
+        // A bucket holding three or more symbols (the distribution tails,
+        // 1-4% of lanes): the team resolves such lanes one at a time, each
+        // thread testing one candidate symbol of that lane's channel, so T
+        // symbols are passed per ballot.
+        if (__any_sync(tm, slow != 0)) {
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            uint32_t bal = __ballot_sync(tm, (slow >> j) & 1u) & tm;
+            while (bal) {
+              const int src = __ffs(bal) - 1;
+              bal &= bal - 1;
+              const uint32_t sl = __shfl_sync(tm, x[j] & 0xFFFFu, src);
+              uint32_t sb = __shfl_sync(tm, sy[j], src) + 1;  // s0 and s0+1 are excluded
+              const uint16_t *row = crow + (kLpt * (src % T) + j) * 256;
+              uint32_t nb;
+              do {
+                const uint32_t sc = sb + i;
+                const bool below = sc < 255 && row[sc + 1] <= sl;
+                nb = __popc(__ballot_sync(tm, below) & tm);
+                sb += nb;
+              } while (nb == T);
+              if ((threadIdx.x & 31) == src) {
+                sy[j] = sb;
+                ee[j] = et[(sb * kLpt + j) * T];
+                rr[j] = sl - (ee[j] & 0xFFFFu);
+              }
             }
           }
-          x[j] = (e >> 16) * (x[j] >> 16) + r;
-          sym[j] = s;
-          need[j] = x[j] < kRansL ? 1u : 0u;
-          cntw += int(need[j]) + (s == kEsc ? 2 : 0);
         }
+        uint32_t needm = 0, escm = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          x[j] = (ee[j] >> 16) * (x[j] >> 16) + rr[j];
+          needm |= (x[j] < kRansL) ? (1u << j) : 0u;
+          escm |= (sy[j] == kEsc) ? (1u << j) : 0u;
+        }
+        const int cntw = __popc(needm) + 2 * __popc(escm);
+        // ---- word positions: team-wide exclusive scan of the word counts
         int incl = cntw;
 #pragma unroll
         for (int o = 1; o < T; o <<= 1) {
@@ -228,26 +261,33 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           break;
         }
         uint32_t pos = p + uint32_t(incl - cntw);
-        float v[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-          if (need[j]) x[j] = (x[j] << 16) | ld_word(words + pos++);
-          int q;
-          if (sym[j] == kEsc) {
-            q = int(uint32_t(ld_word(words + pos)) | (uint32_t(ld_word(words + pos + 1)) << 16));
-            pos += 2;
-            nesc++;
-          } else {
-            q = int(sym[j]) - 127;
-          }
-          float y = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
-          v[j] = fminf(fmaxf(y, -65504.0f), 65504.0f);
-        }
         p += tot;
-        __half2 h01 = __floats2half2_rn(v[0], v[1]);
-        __half2 h23 = __floats2half2_rn(v[2], v[3]);
-        *reinterpret_cast<uint2 *>(out + uint64_t(tr) * lo.d) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
+        if (i == 0 && p + 256 < nw) asm volatile("prefetch.global.L1 [%0];" ::"l"(words + p + 256));
+        float v[4];
+        if (escm == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);  // x<<16 | w
+            // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
+            const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+            v[j] = __fmaf_rn(qf, step[j], ah[j]);
+          }
+        } else {  // escapes: the raw q follows the lane's renormalisation word
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
+            if ((escm >> j) & 1u) {
+              const int q = int(uint32_t(words[pos]) | (uint32_t(words[pos + 1]) << 16));
+              pos += 2;
+              nesc++;
+              v[j] = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
+            } else {
+              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+              v[j] = __fmaf_rn(qf, step[j], ah[j]);
+            }
+          }
+        }
+        *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
       }
     }
 #pragma unroll
@@ -260,10 +300,11 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 template <int T>
 cudaError_t launch_decode_t(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                             uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
-  const size_t smem = size_t(257) * lo.d * 4 + size_t(256) * lo.d;
+  const size_t smem = size_t(257) * lo.d * 4 + size_t(256) * lo.d + size_t(256) * lo.d * 2;
   cudaError_t e = cudaFuncSetAttribute(k_decode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
+  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
   k_decode<T><<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws);
   return cudaGetLastError();
 }
@@ -276,8 +317,7 @@ cudaError_t launch_decode(const Layout &lo, const uint8_t *tables, const uint8_t
   k_decode_index<<<1, 32, 0, st>>>(lo, tables, buf, bytes, k0, k1, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int teams = k1 - k0;
-  if (teams > kMaxTeams) teams = kMaxTeams;
+  const int teams = k1 - k0;
   if (teams < 1) return cudaSuccess;
   switch (lo.d / kLpt) {
     case 2: return launch_decode_t<2>(lo, tables, buf, kv, ws, teams, st);

@@ -57,7 +57,7 @@ constexpr int kLpt = kLanesPerThread;
 
 // ---------------------------------------------------------------- k_encode
 template <int T>
-__global__ void __launch_bounds__(kMaxTeams * T)
+__global__ void __launch_bounds__(max_threads<T>())
 k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv,
          uint8_t *ws) {
   extern __shared__ __align__(16) uint32_t etab[];  // [256][4][T] : cdf | f << 16
@@ -109,57 +109,66 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
 #pragma unroll
       for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
       const int tend = min(g * lo.G + lo.G, ntok);
-      for (int tr = tend - 1; tr > g * lo.G; tr--) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tr) * lo.d));
-        const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-        uint32_t word[4], qv[4];
-        int nem[4];
-        bool esc[4], ren[4];
-        int cntw = 0;
+      // delta tokens of the group in reverse, kAhead rows loaded at a time
+      constexpr int kAhead = 4;
+      for (int tb = tend - 1; tb > g * lo.G && !overflow; tb -= kAhead) {
+        const int nb = min(kAhead, tb - g * lo.G);
+        uint2 rows[kAhead];
 #pragma unroll
-        for (int j = 3; j >= 0; j--) {
-          if (((hw[j] >> 10) & 31u) == 31u) bad = true;
-          const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
-          const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
-          esc[j] = !(q >= -R && q <= R);
-          const int sym = esc[j] ? kEsc : q + 127;
-          const uint32_t e = etab[(sym * kLpt + j) * T + i];
-          const uint32_t f = e >> 16, c = e & 0xFFFFu;
-          ren[j] = x[j] >= (f << 16);
-          word[j] = x[j] & 0xFFFFu;
-          uint32_t xr = ren[j] ? (x[j] >> 16) : x[j];
-          x[j] = rans_put(xr, f, c);
-          qv[j] = uint32_t(q);
-          nem[j] = (esc[j] ? 2 : 0) + (ren[j] ? 1 : 0);
-          cntw += nem[j];
-        }
-        // emission order: lanes descending, i.e. threads descending
-        int suf = cntw;
+        for (int u = 0; u < kAhead; u++)
+          if (u < nb) rows[u] = __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tb - u) * lo.d));
 #pragma unroll
-        for (int o = 1; o < T; o <<= 1) {
-          const int v = __shfl_down_sync(tm, suf, o, T);
-          if (i + o < T) suf += v;
-        }
-        const int tot = __shfl_sync(tm, suf, 0, T);
-        if (E + tot > cap) {
-          overflow = true;
-          break;
-        }
-        int64_t e = E + (suf - cntw);
+        for (int u = 0; u < kAhead; u++) {
+          if (u >= nb || overflow) break;
+          const uint2 raw = rows[u];
+          const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+          uint32_t word[4], qv[4];
+          bool esc[4], ren[4];
+          int cntw = 0;
 #pragma unroll
-        for (int j = 3; j >= 0; j--) {
-          if (esc[j]) {
-            wout[cap - 1 - e] = uint16_t(qv[j] >> 16);
-            wout[cap - 2 - e] = uint16_t(qv[j] & 0xFFFFu);
-            e += 2;
-            nesc++;
+          for (int j = 3; j >= 0; j--) {
+            if (((hw[j] >> 10) & 31u) == 31u) bad = true;
+            const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
+            const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
+            esc[j] = !(q >= -R && q <= R);
+            const int sym = esc[j] ? kEsc : q + 127;
+            const uint32_t e = etab[(sym * kLpt + j) * T + i];
+            const uint32_t f = e >> 16, c = e & 0xFFFFu;
+            ren[j] = x[j] >= (f << 16);
+            word[j] = x[j] & 0xFFFFu;
+            const uint32_t xr = ren[j] ? (x[j] >> 16) : x[j];
+            x[j] = rans_put(xr, f, c);
+            qv[j] = uint32_t(q);
+            cntw += (esc[j] ? 2 : 0) + (ren[j] ? 1 : 0);
           }
-          if (ren[j]) {
-            wout[cap - 1 - e] = uint16_t(word[j]);
-            e += 1;
+          // emission order: lanes descending, i.e. threads descending
+          int suf = cntw;
+#pragma unroll
+          for (int o = 1; o < T; o <<= 1) {
+            const int v = __shfl_down_sync(tm, suf, o, T);
+            if (i + o < T) suf += v;
           }
+          const int tot = __shfl_sync(tm, suf, 0, T);
+          if (E + tot > cap) {
+            overflow = true;
+            break;
+          }
+          int64_t e = E + (suf - cntw);
+#pragma unroll
+          for (int j = 3; j >= 0; j--) {
+            if (esc[j]) {
+              wout[cap - 1 - e] = uint16_t(qv[j] >> 16);
+              wout[cap - 2 - e] = uint16_t(qv[j] & 0xFFFFu);
+              e += 2;
+              nesc++;
+            }
+            if (ren[j]) {
+              wout[cap - 1 - e] = uint16_t(word[j]);
+              e += 1;
+            }
+          }
+          E += tot;
         }
-        E += tot;
       }
     }
     if (bad) atomicOr(status, kStNonfinite);
@@ -245,20 +254,22 @@ k_scan_total(Layout lo, EncWs w, uint8_t *ws, uint64_t cap, uint64_t *out_bytes)
 }
 
 // ---------------------------------------------------------------- compaction
+// Fixed parts of all chunks, 16 bytes per thread per step: the chunk
+// header, the scales and anchors from the scratch (which has the container's
+// layout), the stream index, and zero padding.  Block 0 also writes the
+// container header and the chunk index.
 __global__ void __launch_bounds__(256)
 k_compact_fixed(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__restrict__ out) {
   if (*reinterpret_cast<const uint32_t *>(ws + w.status) & (kStCapacity | kStNonfinite)) return;
-  const int k = blockIdx.x;
   const uint64_t *coff = reinterpret_cast<const uint64_t *>(ws + w.coff);
-  const uint64_t base = coff[k];
   const uint8_t *lv8 = ws + w.levels + 4 * kMaxLevels * (1 + uint64_t(lo.n_chunks));
-  if (k == 0) {
-    uint32_t *hd = reinterpret_cast<uint32_t *>(out);
+  if (blockIdx.x == 0) {
     for (uint64_t b = 64 + threadIdx.x * 8; b < lo.hdr_bytes; b += blockDim.x * 8) {
       const uint64_t kk = (b - 64) / 8;
       *reinterpret_cast<uint64_t *>(out + b) = kk < uint64_t(lo.n_chunks) ? coff[kk] : 0;
     }
     if (threadIdx.x == 0) {
+      uint32_t *hd = reinterpret_cast<uint32_t *>(out);
       hd[0] = 0x564B4743u;  // "CGKV"
       hd[1] = 1;
       hd[2] = lo.L;
@@ -275,24 +286,37 @@ k_compact_fixed(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__r
       hd[15] = 0;
     }
   }
-  uint32_t *dst = reinterpret_cast<uint32_t *>(out + base);
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(ws + w.chunks + uint64_t(k) * lo.fixed_full);
-  const uint32_t *soff = reinterpret_cast<const uint32_t *>(ws + w.soff) + uint64_t(k) * lo.nstr;
-  const uint64_t ng = chunk_ng(lo, k);
-  const uint64_t s_end = (lo.sec_s + 4 * uint64_t(lo.nstr) * lo.d) / 4;
-  const uint64_t a_beg = lo.sec_anc / 4, a_end = (lo.sec_anc + uint64_t(lo.nstr) * ng * lo.d) / 4;
-  const uint64_t o_beg = chunk_sec_off(lo, k) / 4, o_end = o_beg + lo.nstr;
-  const uint64_t nwords = chunk_fixed(lo, k) / 4;
-  for (uint64_t u = threadIdx.x; u < nwords; u += blockDim.x) {
-    uint32_t v = 0;
-    if (u == 0) v = lv8[k];
-    else if (u == 1) v = uint32_t(int64_t(k) * lo.C);
-    else if (u == 2) v = uint32_t(chunk_ntok(lo, k));
-    else if (u == 3) v = uint32_t(ng);
-    else if (u < s_end) v = src[u];
-    else if (u >= a_beg && u < a_end) v = src[u];
-    else if (u >= o_beg && u < o_end) v = soff[u - o_beg];
-    dst[u] = v;
+  const uint64_t upc = lo.fixed_full / 16;  // 16-byte units per chunk slot
+  const uint64_t total = upc * uint64_t(lo.n_chunks);
+  const uint32_t *soff_all = reinterpret_cast<const uint32_t *>(ws + w.soff);
+  for (uint64_t u = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += uint64_t(gridDim.x) * blockDim.x) {
+    const int k = int(u / upc);
+    const uint64_t off = (u - uint64_t(k) * upc) * 16;
+    if (off >= chunk_fixed(lo, k)) continue;
+    const uint64_t ng = chunk_ng(lo, k);
+    const uint64_t a_end = lo.sec_anc + uint64_t(lo.nstr) * ng * lo.d;
+    const uint64_t o_beg = chunk_sec_off(lo, k);
+    uint32_t v[4];
+    if (off == 0) {
+      v[0] = lv8[k];
+      v[1] = uint32_t(int64_t(k) * lo.C);
+      v[2] = uint32_t(chunk_ntok(lo, k));
+      v[3] = uint32_t(ng);
+    } else if (off < o_beg) {  // scales, anchors (the scale section has no padding)
+      const uint4 q = *reinterpret_cast<const uint4 *>(ws + w.chunks + uint64_t(k) * lo.fixed_full + off);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+#pragma unroll
+      for (int c = 0; c < 4; c++)
+        if (off >= lo.sec_anc && off + 4 * c >= a_end) v[c] = 0;
+    } else {  // stream index
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const uint64_t wi = (off - o_beg) / 4 + c;
+        v[c] = wi < uint64_t(lo.nstr) ? soff_all[uint64_t(k) * lo.nstr + wi] : 0u;
+      }
+    }
+    *reinterpret_cast<uint4 *>(out + coff[k] + off) = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -327,6 +351,7 @@ cudaError_t launch_encode_t(const Layout &lo, const EncWs &w, const uint8_t *tab
   cudaError_t e = cudaFuncSetAttribute(k_encode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
+  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
   k_encode<T><<<grid, teams * T, smem, st>>>(lo, w, tables, kv, ws);
   return cudaGetLastError();
 }
@@ -335,7 +360,6 @@ cudaError_t launch_encode_t(const Layout &lo, const EncWs &w, const uint8_t *tab
 
 cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,
                           const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
-  if (teams > kMaxTeams) teams = kMaxTeams;
   if (teams < 1) return cudaSuccess;
   switch (lo.d / kLpt) {
     case 2: return launch_encode_t<2>(lo, w, tables, kv, ws, teams, st);
@@ -351,7 +375,11 @@ cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, u
                                 uint64_t cap, uint64_t *out_bytes, cudaStream_t st) {
   k_scan_chunks<<<lo.n_chunks, kScanThreads, 0, st>>>(lo, w, ws);
   k_scan_total<<<1, kScanThreads, 0, st>>>(lo, w, ws, cap, out_bytes);
-  k_compact_fixed<<<lo.n_chunks, 256, 0, st>>>(lo, w, ws, out);
+  {
+    const uint64_t units = (lo.fixed_full / 16) * uint64_t(lo.n_chunks);
+    const uint64_t blocks = (units + 255) / 256;
+    k_compact_fixed<<<unsigned(blocks < 4096 ? (blocks ? blocks : 1) : 4096), 256, 0, st>>>(lo, w, ws, out);
+  }
   const uint64_t ns = uint64_t(lo.n_chunks) * lo.nstr;
   const unsigned grid = unsigned(ns < 65536 ? ns : 65536);
   k_compact_stream<<<grid, 128, 0, st>>>(lo, w, ws, out);

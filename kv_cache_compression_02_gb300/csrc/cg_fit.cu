@@ -76,19 +76,27 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
 #pragma unroll
   for (int i = 0; i < 8; i++) { T[i] = 0; Qlo[i] = 0; Qhi[i] = 0; }
   bool bad = false;
-  for (int64_t t = row; t < lo.S; t += rows) {
-    uint4 v = ld_nc_v4(head + t * lo.d);
+  for (int64_t t0 = row; t0 < lo.S; t0 += 4 * int64_t(rows)) {
+    uint4 vv[4];
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      uint16_t h = half_bits(v, i);
-      if (((h >> 10) & 31u) == 31u) { bad = true; continue; }
-      int64_t X = f16_scaled(h);
-      T[i] += X;
-      uint64_t a = uint64_t(X < 0 ? -X : X);
-      uint64_t lo64 = a * a, hi64 = __umul64hi(a, a);
-      uint64_t s = Qlo[i] + lo64;
-      Qhi[i] += hi64 + (s < lo64 ? 1u : 0u);
-      Qlo[i] = s;
+    for (int u = 0; u < 4; u++) {
+      const int64_t t = t0 + int64_t(u) * rows;
+      vv[u] = t < lo.S ? ld_nc_v4(head + t * lo.d) : make_uint4(0, 0, 0, 0);  // +0 adds nothing
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        uint16_t h = half_bits(vv[u], i);
+        if (((h >> 10) & 31u) == 31u) { bad = true; continue; }
+        int64_t X = f16_scaled(h);
+        T[i] += X;
+        uint64_t a = uint64_t(X < 0 ? -X : X);
+        uint64_t lo64 = a * a, hi64 = __umul64hi(a, a);
+        uint64_t s = Qlo[i] + lo64;
+        Qhi[i] += hi64 + (s < lo64 ? 1u : 0u);
+        Qlo[i] = s;
+      }
     }
   }
   if (bad) atomicOr(status, kStNonfinite);
@@ -256,16 +264,23 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
     int a0 = max(-127, min(127, __float2int_rn(__fmul_rn(xa0, sc0.y))));
     int a1 = max(-127, min(127, __float2int_rn(__fmul_rn(xa1, sc1.y))));
     const float ah0 = __fmul_rn(float(a0), sc0.x), ah1 = __fmul_rn(float(a1), sc1.x);
-    for (int64_t t = ta + 1; t < te; t++) {
-      uint32_t w = __ldg(head + t * dw);
-      float x0 = __half2float(__ushort_as_half(uint16_t(w & 0xFFFF)));
-      float x1 = __half2float(__ushort_as_half(uint16_t(w >> 16)));
-      int q0 = __float2int_rn(__fmul_rn(__fsub_rn(x0, ah0), r0));
-      int q1 = __float2int_rn(__fmul_rn(__fsub_rn(x1, ah1), r1));
-      int s0 = (q0 >= -R && q0 <= R) ? q0 + 127 : kEsc;
-      int s1 = (q1 >= -R && q1 <= R) ? q1 + 127 : kEsc;
-      atomicAdd(&hist[c0 * 257 + s0], 1u);
-      atomicAdd(&hist[(c0 + 1) * 257 + s1], 1u);
+    for (int64_t tb = ta + 1; tb < te; tb += 8) {  // 8 rows in flight
+      uint32_t ws8[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) ws8[u] = (tb + u < te) ? __ldg(head + (tb + u) * dw) : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        if (tb + u >= te) break;
+        const uint32_t w = ws8[u];
+        float x0 = __half2float(__ushort_as_half(uint16_t(w & 0xFFFF)));
+        float x1 = __half2float(__ushort_as_half(uint16_t(w >> 16)));
+        int q0 = __float2int_rn(__fmul_rn(__fsub_rn(x0, ah0), r0));
+        int q1 = __float2int_rn(__fmul_rn(__fsub_rn(x1, ah1), r1));
+        int s0 = (q0 >= -R && q0 <= R) ? q0 + 127 : kEsc;
+        int s1 = (q1 >= -R && q1 <= R) ? q1 + 127 : kEsc;
+        atomicAdd(&hist[c0 * 257 + s0], 1u);
+        atomicAdd(&hist[(c0 + 1) * 257 + s1], 1u);
+      }
     }
   }
   __syncthreads();

@@ -12,7 +12,11 @@ constexpr uint32_t kRansL = 1u << 16;  // lower bound of the rANS state
 constexpr int kEsc = 255;              // escape symbol
 constexpr int kMaxLevels = 8;
 constexpr int kLanesPerThread = 4;     // rANS lanes (channels) per thread
-constexpr int kMaxTeams = 32;          // streams decoded at once per CTA
+constexpr int kMaxTeams = 32;          // streams coded at once per CTA (T < 32)
+// threads per CTA of the coding kernels for teams of T threads; 768 at
+// T = 32 leaves 80 registers per thread
+template <int T>
+constexpr int max_threads() { return T == 32 ? 768 : kMaxTeams * T; }
 
 // status bits in the first word of every workspace
 constexpr uint32_t kStNonfinite = 1u;

@@ -184,3 +184,39 @@ def test_argument_errors_are_synchronous(orc):
     assert cg.cg_encode(cfg, tbd, gu.to_dev(x), np.full(cd.n_chunks, 3, np.uint8), buf,
                         T.zeros(1, dtype=T.int64, device="cuda"),
                         cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_ENCODE))) == cg.CG_ERR_INVALID_ARG
+
+
+def _special_kv():
+    """Constant channels, +-65504 extremes (reconstructions beyond the fp16
+    range must clamp), subnormals and signed zeros."""
+    f16 = lambda v: np.float16(v).view(np.uint16).item()  # noqa: E731
+    L, H, d, S = 1, 1, 8, 60
+    x = np.zeros((L, 2, H, S, d), np.uint16)
+    x[..., 0] = f16(7.0)
+    x[..., 1] = np.array([f16(65504), f16(-65504)] * 30)
+    x[..., 2] = np.array([1, 0x8001, 3, 0x8000] * 15, np.uint16)
+    x[..., 3] = f16(-0.0)
+    x[..., 4] = np.array([f16(v) for v in np.linspace(-3, 3, S)])
+    x[..., 5] = np.array(([f16(65504)] * 29 + [f16(-65504)]) * 2)
+    x[..., 6] = np.array([f16(65504 - 32 * (t % 3)) for t in range(S)])
+    x[..., 7] = np.array([f16(-65504 + 32 * (t % 5)) for t in range(S)])
+    return x
+
+
+@pytest.mark.parametrize("R,lb", [(127, (0.1,)), (127, (2.0,)), (3, (0.4,))])
+def test_special_values_bit_exact(orc, R, lb):
+    x = _special_kv()
+    L, _, H, S, d = x.shape
+    cd = orc.Codec(L, H, d, S, C=30, G=10, R=R)
+    cfg = cg.Config(L, H, d, S, 30, G=10, R=R, level_base=lb)
+    rc, tb_ref = orc.fit_tables(cd, list(lb), None, x)
+    assert rc == 0
+    st, tb = gu.fit(cfg, x)
+    assert st == cg.CG_OK and np.array_equal(tb, tb_ref)
+    rc, cont_ref, _ = orc.encode(cd, 1, tb_ref, x, np.zeros(cd.n_chunks, np.uint8))
+    st, cont, n = gu.encode(cfg, tb_ref, x, np.zeros(cd.n_chunks, np.uint8))
+    assert st == cg.CG_OK and np.array_equal(cont, cont_ref)
+    rc, y_ref = orc.decode(tb_ref, cont_ref)
+    st, y = gu.decode(cfg, tb_ref, cont_ref)
+    assert rc == 0 and st == cg.CG_OK and np.array_equal(y, y_ref)
+    assert (np.abs(y.view(np.float16).astype(np.float32)) <= 65504).all()
