@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             "cg_decode": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                          P, P, S, P]),
             "cg_read_status": (ctypes.c_int, [P]),
+            "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                                 P, P, ctypes.POINTER(ctypes.c_void_p)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -69,7 +71,11 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(t) -> int:
-    return 0 if t is None else int(t.data_ptr())
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
 
 
 def _stream(s) -> int | None:
@@ -143,6 +149,18 @@ def cg_decode(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: int, chu
     return lib().cg_decode(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(tables), _ptr(bitstream),
                            int(nbytes), int(chunk_begin), int(chunk_end), _ptr(kv), _ptr(ws),
                            ws.numel() * ws.element_size(), _stream(stream))
+
+
+def cg_decode_noalloc(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: int, chunk_end: int, kv,
+                      stream=None):
+    """cg_decode without a workspace (for callers that cannot allocate).
+    Returns (status, device address of the library's scratch, for
+    cg_read_status)."""
+    addr = ctypes.c_void_p(0)
+    rc = lib().cg_decode_noalloc(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(tables), _ptr(bitstream),
+                                 int(nbytes), int(chunk_begin), int(chunk_end), _ptr(kv), _stream(stream),
+                                 ctypes.byref(addr))
+    return rc, addr.value
 
 
 def cg_read_status(ws) -> int:
