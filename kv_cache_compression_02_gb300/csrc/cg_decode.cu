@@ -95,19 +95,21 @@ __device__ __forceinline__ uint32_t team_mask() {
 }
 
 // ---------------------------------------------------------------- decode
-// Shared memory per CTA (d lanes, T = d/4 threads per team):
-//   etab [257][4][T] u32 : cdf_s | f_s << 16   (s = 256 is a zero sentinel)
-//   lut  [256][T][4] u8  : first symbol whose range holds slot b*256
-// Thread i of a team owns lanes 4i..4i+3; its entries sit at word index
-// (row * T + i), so with T = 32 every access of thread i hits bank i.
+// Shared memory per CTA (d lanes, T = d/4 threads per team), 197 KB at d=128:
+//   lut16 [256 buckets][4 lanes x T] u16 : s0 | (last offset of s0 in bucket) << 8
+//   cdfc  [257 symbols][4 lanes x T] u16 : cdf_s (cdf_256 = 2^16 stored as 0)
+//   crow  [d][256] u16                   : cdf rows, for the cooperative search
+// Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
+// (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
+// access of thread i to lut16 or cdfc hits bank i.
 template <int T>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws) {
   extern __shared__ __align__(16) uint32_t smem[];
-  uint32_t *etab = smem;
-  uint8_t *lut = reinterpret_cast<uint8_t *>(smem + 257 * kLpt * T);
-  uint16_t *crow = reinterpret_cast<uint16_t *>(lut + 256 * kLpt * T);  // [d][256] cdf, row layout
+  uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [256][2][T][2]
+  uint16_t *cdfc = lut16 + 256 * kLpt * T;                           // [257][2][T][2]
+  uint16_t *crow = cdfc + 257 * kLpt * T;                            // [d][256]
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
@@ -128,11 +130,14 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     const uint32_t c1 = s < 255 ? cdf[c * 256 + s + 1] : kM;
     if (c1 <= c0 || (s == 0 && c0 != 0)) s_bad = 1;
     const int j = c % kLpt, ti = c / kLpt;
-    etab[(s * kLpt + j) * T + ti] = c0 | ((c1 - c0) << 16);
+    const int col = (j >> 1) * T * 2 + ti * 2 + (j & 1);  // u16 index within a row
+    cdfc[s * (kLpt * T) + col] = uint16_t(c0);
+    if (s == 0) cdfc[256 * (kLpt * T) + col] = 0;  // cdf_256 = 2^16, stored mod 2^16
     crow[c * 256 + s] = uint16_t(c0);
-    if (s == 0) etab[(256 * kLpt + j) * T + ti] = 0;
-    for (uint32_t b = (c0 + 255) >> 8; b <= ((c1 - 1) >> 8) && c1 > c0; b++)
-      lut[(b * T + ti) * kLpt + j] = uint8_t(s);
+    for (uint32_t b = (c0 + 255) >> 8; b <= ((c1 - 1) >> 8) && c1 > c0; b++) {
+      const uint32_t bnd = min(c1 - 256 * b, 256u) - 1;  // slots of s inside bucket b, minus 1
+      lut16[b * (kLpt * T) + col] = uint16_t(s | (bnd << 8));
+    }
   }
   __syncthreads();
   if (s_bad) {
@@ -145,8 +150,10 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   const float4 st4 = *reinterpret_cast<const float4 *>(
       reinterpret_cast<const float *>(tables + lo.tb_step) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
   const float step[4] = {st4.x, st4.y, st4.z, st4.w};
-  const uint32_t *et = etab + i;                 // + (s*4 + j) * T
-  const uint8_t *lt = lut + i * kLpt;            // + b * T * 4 + j
+  // thread i's entries: u16 index row * (4T) + (j>>1)*2T + 2i + (j&1); with
+  // T = 32 a row is 256 bytes, so the bucket row of state x is x & 0xFF00.
+  const uint16_t *lt = lut16 + 2 * i;
+  const uint16_t *ct = cdfc + 2 * i;
 
   for (int idx = team; idx < cnt; idx += nteams) {
     const int k = list[idx];
@@ -194,27 +201,27 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
       orow += lo.d;
       const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
       for (int tt = 0; tt < nt; tt++, orow += lo.d) {
-        // ---- symbol search: bucket LUT, then at most one step forward
-        uint32_t sy[4], ee[4], rr[4];
+        // ---- symbol search.  The bucket entry holds the first symbol s0 of
+        // bucket slot>>8 and the last in-bucket offset of its range, so one
+        // compare picks s0 or s0+1; lanes whose bucket holds 3+ symbols
+        // (distribution tails) are marked slow and resolved below.
+        uint32_t sy[4], ff[4], rr[4];
         uint32_t slow = 0;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
-          const uint32_t slot = x[j] & 0xFFFFu;
-          const uint32_t s0 = lt[((x[j] >> 8) & 0xFFu) * (T * kLpt) + j];  // bucket = slot >> 8
-          const uint32_t e0 = et[(s0 * kLpt + j) * T];
-          const uint32_t e1 = et[((s0 + 1) * kLpt + j) * T];
-          const uint32_t r0 = slot - (e0 & 0xFFFFu);
-          const uint32_t f0 = e0 >> 16;
-          const bool p = r0 >= f0;
-          rr[j] = p ? r0 - f0 : r0;
-          ee[j] = p ? e1 : e0;
-          sy[j] = s0 + (p ? 1u : 0u);
-          slow |= (p && rr[j] >= (e1 >> 16)) ? (1u << j) : 0u;
+          const int cj = (j >> 1) * T * 2 + (j & 1);
+          const uint32_t lu = lt[((x[j] >> 8) & 0xFFu) * (kLpt * T) + cj];
+          const uint32_t sj = (lu & 0xFFu) + (((x[j] & 0xFFu) > (lu >> 8)) ? 1u : 0u);
+          const uint32_t c0 = ct[sj * (kLpt * T) + cj];
+          const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
+          ff[j] = (c1 - c0) & 0xFFFFu;
+          rr[j] = (x[j] & 0xFFFFu) - c0;
+          sy[j] = sj;
+          slow |= (rr[j] >= ff[j]) ? (1u << j) : 0u;
         }
-        // A bucket holding three or more symbols (the distribution tails,
-        // 1-4% of lanes): the team resolves such lanes one at a time, each
-        // thread testing one candidate symbol of that lane's channel, so T
-        // symbols are passed per ballot.
+        // Slow lanes (1-4% of lanes) are resolved by the team, one at a
+        // time: each thread tests one candidate symbol of that lane's
+        // channel, so T symbols are passed per ballot.
         if (__any_sync(tm, slow != 0)) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
@@ -223,7 +230,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
               const int src = __ffs(bal) - 1;
               bal &= bal - 1;
               const uint32_t sl = __shfl_sync(tm, x[j] & 0xFFFFu, src);
-              uint32_t sb = __shfl_sync(tm, sy[j], src) + 1;  // s0 and s0+1 are excluded
+              uint32_t sb = __shfl_sync(tm, sy[j], src) + 1;  // symbols up to sy are excluded
               const uint16_t *row = crow + (kLpt * (src % T) + j) * 256;
               uint32_t nb;
               do {
@@ -233,9 +240,12 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
                 sb += nb;
               } while (nb == T);
               if ((threadIdx.x & 31) == src) {
+                const int cj = (j >> 1) * T * 2 + (j & 1);
+                const uint32_t c0 = ct[sb * (kLpt * T) + cj];
+                const uint32_t c1 = ct[(sb + 1) * (kLpt * T) + cj];
                 sy[j] = sb;
-                ee[j] = et[(sb * kLpt + j) * T];
-                rr[j] = sl - (ee[j] & 0xFFFFu);
+                ff[j] = (c1 - c0) & 0xFFFFu;
+                rr[j] = sl - c0;
               }
             }
           }
@@ -243,7 +253,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         uint32_t needm = 0, escm = 0;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
-          x[j] = (ee[j] >> 16) * (x[j] >> 16) + rr[j];
+          x[j] = ff[j] * (x[j] >> 16) + rr[j];
           needm |= (x[j] < kRansL) ? (1u << j) : 0u;
           escm |= (sy[j] == kEsc) ? (1u << j) : 0u;
         }
@@ -300,7 +310,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 template <int T>
 cudaError_t launch_decode_t(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                             uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
-  const size_t smem = size_t(257) * lo.d * 4 + size_t(256) * lo.d + size_t(256) * lo.d * 2;
+  const size_t smem = size_t(256 + 257 + 256) * lo.d * 2;
   cudaError_t e = cudaFuncSetAttribute(k_decode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
