@@ -45,6 +45,22 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// 16-byte asynchronous global->shared copy that reads only src_bytes (0..16)
+// and zero-fills the rest, so a copy never reads past the stream's words.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint32_t src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gsrc), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Words staged per team: a ring of kRing words in two halves.
+constexpr uint32_t kRing = 512, kHalf = 256;
+// Symbol-search buckets: slot >> kBucketShift, kBuckets of them.
+constexpr uint32_t kBucketShift = 7, kBuckets = 1u << (16 - kBucketShift), kBucketSlots = 1u << kBucketShift;
+constexpr uint32_t kCdfRows = 258;  // cdf_0 .. cdf_257 (the last two stored as 0)
+
 // ---------------------------------------------------------------- index
 __global__ void k_decode_index(Layout lo, const uint8_t *__restrict__ tables,
                                const uint8_t *__restrict__ buf, uint64_t bytes, int32_t k0,
@@ -95,21 +111,23 @@ __device__ __forceinline__ uint32_t team_mask() {
 }
 
 // ---------------------------------------------------------------- decode
-// Shared memory per CTA (d lanes, T = d/4 threads per team), 197 KB at d=128:
-//   lut16 [256 buckets][4 lanes x T] u16 : s0 | (last offset of s0 in bucket) << 8
-//   cdfc  [257 symbols][4 lanes x T] u16 : cdf_s (cdf_256 = 2^16 stored as 0)
-//   crow  [d][256] u16                   : cdf rows, for the cooperative search
+// Shared memory per CTA (d lanes, T = d/4 threads per team), 217 KB at d=128
+// with 22 teams:
+//   lut16 [512 buckets][4 lanes x T] u16 : s0 << 8 | (255 - last offset of s0
+//                                          in the 128-slot bucket)
+//   cdfc  [258 rows][4 lanes x T] u16    : cdf_s (cdf_256 = 2^16 stored as 0)
+//   rings [teams][512] u16               : the staged words of each team
 // Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
-// access of thread i to lut16 or cdfc hits bank i.
+// access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
 template <int T>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws) {
   extern __shared__ __align__(16) uint32_t smem[];
-  uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [256][2][T][2]
-  uint16_t *cdfc = lut16 + 256 * kLpt * T;                           // [257][2][T][2]
-  uint16_t *crow = cdfc + 257 * kLpt * T;                            // [d][256]
+  uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [kBuckets][2][T][2]
+  uint16_t *cdfc = lut16 + kBuckets * kLpt * T;                      // [kCdfRows][2][T][2]
+  uint16_t *rings = cdfc + kCdfRows * kLpt * T;                      // [teams][kRing] words
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
@@ -132,11 +150,13 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     const int j = c % kLpt, ti = c / kLpt;
     const int col = (j >> 1) * T * 2 + ti * 2 + (j & 1);  // u16 index within a row
     cdfc[s * (kLpt * T) + col] = uint16_t(c0);
-    if (s == 0) cdfc[256 * (kLpt * T) + col] = 0;  // cdf_256 = 2^16, stored mod 2^16
-    crow[c * 256 + s] = uint16_t(c0);
-    for (uint32_t b = (c0 + 255) >> 8; b <= ((c1 - 1) >> 8) && c1 > c0; b++) {
-      const uint32_t bnd = min(c1 - 256 * b, 256u) - 1;  // slots of s inside bucket b, minus 1
-      lut16[b * (kLpt * T) + col] = uint16_t(s | (bnd << 8));
+    if (s == 0) {  // cdf_256 = 2^16 (and a padding row), stored mod 2^16
+      cdfc[256 * (kLpt * T) + col] = 0;
+      cdfc[257 * (kLpt * T) + col] = 0;
+    }
+    for (uint32_t b = (c0 + kBucketSlots - 1) >> kBucketShift; b <= ((c1 - 1) >> kBucketShift) && c1 > c0; b++) {
+      const uint32_t bnd = min(c1 - kBucketSlots * b, kBucketSlots) - 1;  // last slot of s in bucket b
+      lut16[b * (kLpt * T) + col] = uint16_t((s << 8) | (255 - bnd));
     }
   }
   __syncthreads();
@@ -184,6 +204,21 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     const uint4 xs = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * i);
     uint32_t x[4] = {xs.x, xs.y, xs.z, xs.w};
     const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
+    // stage the first kRing words (two halves) of the stream in the ring
+    uint16_t *ring = rings + team * kRing;
+    const uint32_t wbytes = 2 * nw;
+    auto load_half = [&](uint32_t w0) {  // words [w0, w0 + kHalf) -> ring half
+      for (uint32_t o = 16 * i; o < 2 * kHalf; o += 16 * T) {
+        const uint32_t b = 2 * w0 + o;  // byte offset in the word array
+        const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
+        cp_async16(ring + ((w0 + o / 2) & (kRing - 1)), reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
+      }
+      cp_async_commit();
+    };
+    __syncwarp(tm);  // the previous stream's reads of this ring are done
+    load_half(0);
+    load_half(kHalf);
+    uint32_t rbase = 0;  // the ring holds words [rbase, rbase + kRing)
     const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
     const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
@@ -192,8 +227,10 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     bool broken = false;
 
     uint16_t *orow = out;
+    uint32_t a4n = *reinterpret_cast<const uint32_t *>(anc);  // next group's anchors, loaded ahead
     for (int g = 0; g < ng && !broken; g++) {
-      const uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
+      const uint32_t a4 = a4n;
+      if (g + 1 < ng) a4n = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g + 1) * lo.d);
       float ah[4];
 #pragma unroll
       for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
@@ -210,8 +247,10 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           const int cj = (j >> 1) * T * 2 + (j & 1);
-          const uint32_t lu = lt[((x[j] >> 8) & 0xFFu) * (kLpt * T) + cj];
-          const uint32_t sj = (lu & 0xFFu) + (((x[j] & 0xFFu) > (lu >> 8)) ? 1u : 0u);
+          const uint32_t b = (x[j] >> kBucketShift) & (kBuckets - 1);
+          const uint32_t lu = lt[b * (kLpt * T) + cj];
+          // carry out of the low byte adds one when the slot is past s0's part of the bucket
+          const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
           const uint32_t c0 = ct[sj * (kLpt * T) + cj];
           const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
           ff[j] = (c1 - c0) & 0xFFFFu;
@@ -219,34 +258,28 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           sy[j] = sj;
           slow |= (rr[j] >= ff[j]) ? (1u << j) : 0u;
         }
-        // Slow lanes (1-4% of lanes) are resolved by the team, one at a
-        // time: each thread tests one candidate symbol of that lane's
-        // channel, so T symbols are passed per ballot.
-        if (__any_sync(tm, slow != 0)) {
+        // A bucket holding three or more symbols (the distribution tails,
+        // about 1% of lanes): binary search between the chosen symbol and the
+        // first symbol of the next bucket, in the lane's own table column.
+        if (slow) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            uint32_t bal = __ballot_sync(tm, (slow >> j) & 1u) & tm;
-            while (bal) {
-              const int src = __ffs(bal) - 1;
-              bal &= bal - 1;
-              const uint32_t sl = __shfl_sync(tm, x[j] & 0xFFFFu, src);
-              uint32_t sb = __shfl_sync(tm, sy[j], src) + 1;  // symbols up to sy are excluded
-              const uint16_t *row = crow + (kLpt * (src % T) + j) * 256;
-              uint32_t nb;
-              do {
-                const uint32_t sc = sb + i;
-                const bool below = sc < 255 && row[sc + 1] <= sl;
-                nb = __popc(__ballot_sync(tm, below) & tm);
-                sb += nb;
-              } while (nb == T);
-              if ((threadIdx.x & 31) == src) {
-                const int cj = (j >> 1) * T * 2 + (j & 1);
-                const uint32_t c0 = ct[sb * (kLpt * T) + cj];
-                const uint32_t c1 = ct[(sb + 1) * (kLpt * T) + cj];
-                sy[j] = sb;
-                ff[j] = (c1 - c0) & 0xFFFFu;
-                rr[j] = sl - c0;
+            if ((slow >> j) & 1u) {
+              const int cj = (j >> 1) * T * 2 + (j & 1);
+              const uint32_t slot = x[j] & 0xFFFFu;
+              const uint32_t b = slot >> kBucketShift;
+              uint32_t lo = sy[j] + 1;  // cdf_lo <= slot is known
+              uint32_t hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
+              while (lo < hi) {
+                const uint32_t mid = (lo + hi + 1) >> 1;
+                if (ct[mid * (kLpt * T) + cj] <= slot) lo = mid;
+                else hi = mid - 1;
               }
+              const uint32_t c0 = ct[lo * (kLpt * T) + cj];
+              const uint32_t c1 = ct[(lo + 1) * (kLpt * T) + cj];
+              sy[j] = lo;
+              ff[j] = (c1 - c0) & 0xFFFFu;
+              rr[j] = slot - c0;
             }
           }
         }
@@ -271,9 +304,45 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           break;
         }
         uint32_t pos = p + uint32_t(incl - cntw);
+        // make words [p, p + tot) available in the ring
+        if (p >= rbase + kHalf) {
+          __syncwarp(tm);  // every thread's reads of the consumed half are done
+          do {  // first half consumed: refill it with the next words
+            load_half(rbase + kRing);
+            rbase += kHalf;
+          } while (p >= rbase + kHalf);
+        }
+        const bool in_ring = p + tot <= rbase + kRing;
+        if (p + tot <= rbase + kHalf) cp_async_wait_prev();
+        else cp_async_wait_all();
+        __syncwarp(tm);
         p += tot;
-        if (i == 0 && p + 256 < nw) asm volatile("prefetch.global.L1 [%0];" ::"l"(words + p + 256));
         float v[4];
+        if (in_ring) {
+        if (escm == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(ring[pos++ & (kRing - 1)]), x[j], 0x5410);  // x<<16 | w
+            // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
+            const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+            v[j] = __fmaf_rn(qf, step[j], ah[j]);
+          }
+        } else {  // escapes: the raw q follows the lane's renormalisation word
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(ring[pos++ & (kRing - 1)]), x[j], 0x5410);
+            if ((escm >> j) & 1u) {
+              const int q = int(uint32_t(ring[pos & (kRing - 1)]) | (uint32_t(ring[(pos + 1) & (kRing - 1)]) << 16));
+              pos += 2;
+              nesc++;
+              v[j] = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
+            } else {
+              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+              v[j] = __fmaf_rn(qf, step[j], ah[j]);
+            }
+          }
+        }
+        } else {  // a burst longer than the ring: straight from memory
         if (escm == 0) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
@@ -297,9 +366,11 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             }
           }
         }
+        }
         *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
       }
     }
+    cp_async_wait_all();
 #pragma unroll
     for (int o = T / 2; o; o >>= 1) nesc += __shfl_xor_sync(tm, nesc, o, T);
     const bool lanes_ok = x[0] == kRansL && x[1] == kRansL && x[2] == kRansL && x[3] == kRansL;
@@ -310,11 +381,11 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 template <int T>
 cudaError_t launch_decode_t(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                             uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
-  const size_t smem = size_t(256 + 257 + 256) * lo.d * 2;
+  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
+  const size_t smem = size_t(kBuckets + kCdfRows) * lo.d * 2 + size_t(teams) * kRing * 2;
   cudaError_t e = cudaFuncSetAttribute(k_decode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
-  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
   k_decode<T><<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws);
   return cudaGetLastError();
 }
