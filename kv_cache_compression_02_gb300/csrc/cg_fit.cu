@@ -33,14 +33,6 @@ __device__ __forceinline__ uint16_t half_bits(const uint4 &v, int i) {
   return uint16_t((i & 1) ? (w >> 16) : (w & 0xFFFF));
 }
 
-// fp16 value times 2^24 as an exact integer (|X| < 2^40)
-__device__ __forceinline__ int64_t f16_scaled(uint16_t h) {
-  uint32_t e = (h >> 10) & 31u;
-  uint64_t m = h & 1023u;
-  uint64_t v = e ? ((m | 1024u) << (e - 1)) : m;
-  return (h & 0x8000u) ? -int64_t(v) : int64_t(v);
-}
-
 // unsigned 128-bit integer to binary64, round to nearest even.  The top 64
 // bits (with the leading one at bit 63) carry the rounding; any nonzero bit
 // below them is folded into the lowest bit as a sticky bit, which lies
@@ -56,46 +48,56 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 }
 
 // ---------------------------------------------------------------- k_stats
-// One CTA per head; each thread owns 8 channels (one 16-byte load per token)
-// and a strided subset of the tokens.  Integer sums are order-free, so the
+// One CTA per head; each thread owns 4 channels (one 8-byte load per token)
+// and a strided subset of the tokens.  An fp16 value is X = M * 2^E (times
+// 2^-24) with M < 2^11, so X^2 = M^2 << 2E is one 32-bit multiply and a
+// shifted add into a 128-bit sum.  Integer sums are order-free, so the
 // reduction order does not matter for the result.
-constexpr int kStatsThreads = 256;
+constexpr int kStatsThreads = 512;
+
+__device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint64_t &Qlo, uint64_t &Qhi) {
+  const uint32_t e = (h >> 10) & 31u;
+  const uint32_t M = e ? ((h & 1023u) | 1024u) : (h & 1023u);
+  const uint32_t E = e ? e - 1 : 0;  // X = M << E
+  const int64_t X = int64_t(uint64_t(M) << E);
+  T += (h & 0x8000u) ? -X : X;
+  const uint32_t m2 = M * M;  // < 2^22
+  const uint32_t sh = 2 * E;  // 0..58
+  const uint64_t lo = uint64_t(m2) << sh;                         // low 64 bits of m2 << sh
+  const uint32_t hi = sh > 42 ? (m2 >> (64 - sh)) : 0u;           // bits 64.. of m2 << sh
+  Qlo += lo;
+  Qhi += uint64_t(hi) + (Qlo < lo ? 1u : 0u);
+}
 
 __global__ void __launch_bounds__(kStatsThreads)
 k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables,
         const float *__restrict__ mult, Bases bases, uint32_t *status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int si = blockIdx.x;
-  const int tpr = lo.d / 8;                 // threads per token row
+  const int tpr = lo.d / 4;                 // threads per token row
   const int rows = kStatsThreads / tpr;     // token rows in flight
   const int col = threadIdx.x % tpr, row = threadIdx.x / tpr;
-  const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 8 * col;
+  const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 4 * col;
 
-  int64_t T[8];
-  uint64_t Qlo[8], Qhi[8];
+  int64_t T[4];
+  uint64_t Qlo[4], Qhi[4];
 #pragma unroll
-  for (int i = 0; i < 8; i++) { T[i] = 0; Qlo[i] = 0; Qhi[i] = 0; }
-  bool bad = false;
+  for (int i = 0; i < 4; i++) { T[i] = 0; Qlo[i] = 0; Qhi[i] = 0; }
+  uint32_t bad = 0;
   for (int64_t t0 = row; t0 < lo.S; t0 += 4 * int64_t(rows)) {
-    uint4 vv[4];
+    uint2 vv[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const int64_t t = t0 + int64_t(u) * rows;
-      vv[u] = t < lo.S ? ld_nc_v4(head + t * lo.d) : make_uint4(0, 0, 0, 0);  // +0 adds nothing
+      vv[u] = t < lo.S ? __ldg(reinterpret_cast<const uint2 *>(head + t * lo.d)) : make_uint2(0, 0);
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
+      const uint32_t hw[4] = {vv[u].x & 0xFFFFu, vv[u].x >> 16, vv[u].y & 0xFFFFu, vv[u].y >> 16};
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        uint16_t h = half_bits(vv[u], i);
-        if (((h >> 10) & 31u) == 31u) { bad = true; continue; }
-        int64_t X = f16_scaled(h);
-        T[i] += X;
-        uint64_t a = uint64_t(X < 0 ? -X : X);
-        uint64_t lo64 = a * a, hi64 = __umul64hi(a, a);
-        uint64_t s = Qlo[i] + lo64;
-        Qhi[i] += hi64 + (s < lo64 ? 1u : 0u);
-        Qlo[i] = s;
+      for (int i = 0; i < 4; i++) {
+        bad |= (hw[i] & 0x7C00u) == 0x7C00u;
+        acc_moments(hw[i], T[i], Qlo[i], Qhi[i]);  // a non-finite value only spoils a flagged result
       }
     }
   }
@@ -105,8 +107,8 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   uint64_t *sQl = reinterpret_cast<uint64_t *>(sT + rows * lo.d);
   uint64_t *sQh = sQl + rows * lo.d;
 #pragma unroll
-  for (int i = 0; i < 8; i++) {
-    int c = 8 * col + i;
+  for (int i = 0; i < 4; i++) {
+    const int c = 4 * col + i;
     sT[row * lo.d + c] = T[i];
     sQl[row * lo.d + c] = Qlo[i];
     sQh[row * lo.d + c] = Qhi[i];
@@ -229,7 +231,7 @@ k_anchor(Layout lo, const uint16_t *__restrict__ kv, float2 *__restrict__ scale_
 // chunk's scale, quantizes the group's deltas and counts the symbols into
 // a shared [d][257] histogram (the odd row stride spreads channels over
 // banks).  Then one warp per channel normalises its counts.
-constexpr int kHistThreads = 512;
+constexpr int kHistThreads = 1024;
 
 __global__ void __launch_bounds__(kHistThreads)
 k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ scale,
@@ -348,8 +350,10 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
 
 cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
                          Bases bases, uint32_t *status, cudaStream_t st) {
-  const int rows = kStatsThreads / (lo.d / 8);
+  const int rows = kStatsThreads / (lo.d / 4);
   const size_t smem = size_t(rows) * lo.d * 24;
+  cudaError_t e = cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
   k_stats<<<lo.nstr, kStatsThreads, smem, st>>>(lo, kv, tables, mult, bases, status);
   return cudaGetLastError();
 }
