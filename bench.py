@@ -142,7 +142,7 @@ def cpu_oracle_decode_rate(w, host_np, budget_s=10.0):
     L, H, S, d = w.L, w.H, w.S, w.d
     spent, nbytes, streams = 0.0, 0, 0
     heads = L * 2 * H
-    step_ = max(1, heads // 16)
+    step_ = max(1, heads // 128)
     out = np.zeros((S, d), np.uint16)
     for si in range(0, heads, step_):
         l = si // (2 * H)
@@ -357,7 +357,7 @@ def main():
         "ratio": fp16 / nbytes, "ratio_incl_tables": fp16 / (nbytes + tb_bytes),
         "container_bytes": nbytes, "tables_bytes": tb_bytes,
         "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": peak, "unit": "GB/s", "frac": dec_ach / peak,
-                     "traffic": traffic_for("k_decode", 1.0), "kernel": "cg_decode",
+                     "traffic": traffic_for("k_decode", fp16), "kernel": "cg_decode",
                      "algorithmic_bytes_per_launch": dec_alg, "peak_kind": peak_kind,
                      "frac_of_8TBs": dec_ach / 8000.0},
         "roofline_encode": {"bound": "hbm", "achieved": enc_ach, "peak": peak, "unit": "GB/s",
