@@ -219,6 +219,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     load_half(0);
     load_half(kHalf);
     uint32_t rbase = 0;  // the ring holds words [rbase, rbase + kRing)
+    uint32_t ready = 0;  // words [rbase, ready) have landed and are visible to the team
     const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
     const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
@@ -313,16 +314,28 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           } while (p >= rbase + kHalf);
         }
         const bool in_ring = p + tot <= rbase + kRing;
-        if (p + tot <= rbase + kHalf) cp_async_wait_prev();
-        else cp_async_wait_all();
-        __syncwarp(tm);
+        if (p + tot > ready) {  // words past what is known to have landed
+          if (p + tot <= rbase + kHalf) {
+            cp_async_wait_prev();
+            ready = rbase + kHalf;
+          } else {
+            cp_async_wait_all();
+            ready = rbase + kRing;
+          }
+          __syncwarp(tm);
+        }
         p += tot;
         float v[4];
         if (in_ring) {
         if (escm == 0) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(ring[pos++ & (kRing - 1)]), x[j], 0x5410);  // x<<16 | w
+            {
+              const uint32_t w = ring[pos & (kRing - 1)];  // read unconditionally, use if needed
+              const bool nd = (needm >> j) & 1u;
+              x[j] = nd ? __byte_perm(w, x[j], 0x5410) : x[j];  // x<<16 | w
+              pos += nd ? 1u : 0u;
+            }
             // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
             const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
             v[j] = __fmaf_rn(qf, step[j], ah[j]);
