@@ -320,6 +320,39 @@ k_compact_fixed(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__r
   }
 }
 
+// Stream blocks: header, states, then the words copied 16 bytes at a time.
+// The scratch words of a stream end on a 16-byte boundary but start anywhere
+// (2-byte steps), so each 16-byte output is assembled from two aligned
+// 16-byte loads with a funnel shift; bytes past the last word are zero.
+template <int OFS, int SH>
+__device__ __forceinline__ uint4 shifted16(const uint4 &a, const uint4 &b) {
+  const uint32_t q[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) r[k] = SH ? __funnelshift_r(q[k + OFS], q[k + OFS + 1], SH) : q[k + OFS];
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+template <int OFS, int SH>
+__device__ void copy_words(uint8_t *dst, const uint8_t *src_aligned, uint64_t nbytes, uint64_t nout) {
+  for (uint64_t o = threadIdx.x * 16ull; o < nout; o += blockDim.x * 16ull) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(src_aligned + o);
+    const uint4 b = *reinterpret_cast<const uint4 *>(src_aligned + o + 16);
+    uint4 v = shifted16<OFS, SH>(a, b);
+    if (o + 16 > nbytes) {  // last piece: zero the padding
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint64_t bo = o + 4 * k;
+        if (bo >= nbytes) w[k] = 0;
+        else if (bo + 4 > nbytes) w[k] &= 0xFFFFu;  // one 2-byte word left in this 4-byte slot
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4 *>(dst + o) = v;
+  }
+}
+
 __global__ void __launch_bounds__(128)
 k_compact_stream(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__restrict__ out) {
   if (*reinterpret_cast<const uint32_t *>(ws + w.status) & (kStCapacity | kStNonfinite)) return;
@@ -332,15 +365,26 @@ k_compact_stream(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__
     uint8_t *blk = out + base;
     if (threadIdx.x == 0)
       *reinterpret_cast<uint4 *>(blk) = make_uint4(inf.x, inf.y, uint32_t(chunk_nd(lo, k)), 0u);
-    const uint32_t *st = reinterpret_cast<const uint32_t *>(ws + w.states) + sidx * lo.d;
-    uint32_t *sd = reinterpret_cast<uint32_t *>(blk + 16);
-    for (int j = threadIdx.x; j < lo.d; j += blockDim.x) sd[j] = st[j];
-    const uint16_t *src = reinterpret_cast<const uint16_t *>(ws + w.words) + sidx * w.words_cap +
-                          (w.words_cap - inf.x);
-    uint16_t *wd = reinterpret_cast<uint16_t *>(blk + 16 + 4 * lo.d);
-    const uint64_t end = pad16(16 + 4 * uint64_t(lo.d) + 2 * uint64_t(inf.x));
-    const uint64_t nslots = (end - 16 - 4 * uint64_t(lo.d)) / 2;
-    for (uint64_t u = threadIdx.x; u < nslots; u += blockDim.x) wd[u] = u < inf.x ? src[u] : 0;
+    const uint4 *st = reinterpret_cast<const uint4 *>(ws + w.states + 4 * sidx * lo.d);
+    uint4 *sd = reinterpret_cast<uint4 *>(blk + 16);
+    for (int j = threadIdx.x; j < lo.d / 4; j += blockDim.x) sd[j] = st[j];
+    // words: scratch bytes [so, so + 2 n_words) of this stream's slot
+    const uint8_t *slot = ws + w.words + 2 * sidx * w.words_cap;
+    const uint64_t so = 2 * (w.words_cap - inf.x);
+    const uint64_t nbytes = 2 * uint64_t(inf.x);
+    const uint64_t nout = pad16(16 + 4 * uint64_t(lo.d) + nbytes) - 16 - 4 * uint64_t(lo.d);
+    const uint8_t *src = slot + (so & ~uint64_t(15));
+    uint8_t *dst = blk + 16 + 4 * lo.d;
+    switch (so & 15) {  // the same for the whole stream: no divergence
+      case 0: copy_words<0, 0>(dst, src, nbytes, nout); break;
+      case 2: copy_words<0, 16>(dst, src, nbytes, nout); break;
+      case 4: copy_words<1, 0>(dst, src, nbytes, nout); break;
+      case 6: copy_words<1, 16>(dst, src, nbytes, nout); break;
+      case 8: copy_words<2, 0>(dst, src, nbytes, nout); break;
+      case 10: copy_words<2, 16>(dst, src, nbytes, nout); break;
+      case 12: copy_words<3, 0>(dst, src, nbytes, nout); break;
+      default: copy_words<3, 16>(dst, src, nbytes, nout); break;
+    }
   }
 }
 

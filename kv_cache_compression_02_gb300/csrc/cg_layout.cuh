@@ -138,7 +138,7 @@ inline EncWs enc_ws(const Layout &lo) {
   w.coff = pad256(w.soff + 4 * ns);                                // u64 [nk] + total
   w.words_cap = uint64_t(lo.nd_full) * lo.d * words_per_symbol(lo);
   w.words = pad256(w.coff + 8 * (uint64_t(lo.n_chunks) + 1));      // u16 [ns][cap]
-  w.bytes = pad256(w.words + 2 * ns * w.words_cap);
+  w.bytes = pad256(w.words + 2 * ns * w.words_cap + 32);  // 16-byte reads may run 32 bytes past the last slot
   return w;
 }
 
