@@ -361,7 +361,8 @@ def main():
                      "algorithmic_bytes_per_launch": dec_alg, "peak_kind": peak_kind,
                      "frac_of_8TBs": dec_ach / 8000.0},
         "roofline_encode": {"bound": "hbm", "achieved": enc_ach, "peak": peak, "unit": "GB/s",
-                            "frac": enc_ach / peak, "algorithmic_bytes_per_launch": enc_alg},
+                            "frac": enc_ach / peak, "traffic": traffic_for("k_encode", fp16), "kernel": "cg_encode",
+                            "algorithmic_bytes_per_launch": enc_alg},
         "e2e": {"value": world * fp16 / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": nbytes,
                 "d2h_bytes_per_step": fp16, "what": "pinned-host container -> cg_decode -> pinned-host KV"},
         "gpu_launches": args.steps * (3 + 6 + 2),
