@@ -69,7 +69,7 @@ __device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint64_t &Ql
   Qhi += uint64_t(hi) + (Qlo < lo ? 1u : 0u);
 }
 
-__global__ void __launch_bounds__(kStatsThreads)
+__global__ void __launch_bounds__(kStatsThreads, 2)
 k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables,
         const float *__restrict__ mult, Bases bases, uint32_t *status) {
   extern __shared__ __align__(16) unsigned char smem[];
