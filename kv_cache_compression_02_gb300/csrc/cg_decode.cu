@@ -14,7 +14,7 @@
 //                   team only ever touches bank i (no bank conflicts however
 //                   the symbols fall); each team of d/4 threads decodes one
 //                   chunk's stream, 4 rANS lanes per thread.  Per token: a
-//                   bucket lookup (slot >> 8) plus a forward check finds the
+//                   bucket lookup (slot >> 7) plus one carry finds the
 //                   symbol, a shuffle scan over the team orders the word
 //                   reads, the fused dequantisation fma(q, step, a_hat) is
 //                   clamped, converted to fp16 and stored 8 bytes per thread
@@ -113,9 +113,12 @@ __device__ __forceinline__ uint32_t team_mask() {
 // ---------------------------------------------------------------- decode
 // Shared memory per CTA (d lanes, T = d/4 threads per team), 217 KB at d=128
 // with 22 teams:
-//   lut16 [512 buckets][4 lanes x T] u16 : s0 << 8 | (255 - last offset of s0
-//                                          in the 128-slot bucket)
-//   cdfc  [258 rows][4 lanes x T] u16    : cdf_s (cdf_256 = 2^16 stored as 0)
+//   lut16 [512 buckets][4 lanes x T] u16 : sa << 8 | (255 - last offset of sa
+//                                          in the 128-slot bucket), where
+//                                          (sa, sa + 1) is the neighbouring
+//                                          pair holding most of the bucket
+//   cdfc  [258 rows][4 lanes x T] u16    : cdf_s for s < 256; row 256 repeats
+//                                          cdf_255; row 257 is padding
 //   rings [teams][512] u16               : the staged words of each team
 // Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
@@ -142,21 +145,69 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   __syncthreads();
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
                         tab_index(lo, lv, l, kvi, h * lo.d) * 256;
-  for (int e = threadIdx.x; e < lo.d * 256; e += blockDim.x) {
-    const int c = e >> 8, s = e & 255;
-    const uint32_t c0 = cdf[c * 256 + s];
-    const uint32_t c1 = s < 255 ? cdf[c * 256 + s + 1] : kM;
-    if (c1 <= c0 || (s == 0 && c0 != 0)) s_bad = 1;
-    const int j = c % kLpt, ti = c / kLpt;
-    const int col = (j >> 1) * T * 2 + ti * 2 + (j & 1);  // u16 index within a row
-    cdfc[s * (kLpt * T) + col] = uint16_t(c0);
-    if (s == 0) {  // cdf_256 = 2^16 (and a padding row), stored mod 2^16
-      cdfc[256 * (kLpt * T) + col] = 0;
-      cdfc[257 * (kLpt * T) + col] = 0;
+  constexpr int kRow = kLpt * T;  // u16 entries per table row
+  // u16 position p of a row holds the channel 4 * ti + j with
+  // p = (j >> 1) * 2T + 2 ti + (j & 1)
+  auto chan_of = [](int p) { const int r = p % (2 * T); return 4 * (r >> 1) + 2 * (p / (2 * T)) + (r & 1); };
+  // cdf columns: a thread takes 8 rows of one position (one 16-byte load);
+  // neighbouring threads store neighbouring positions of a row
+  for (int e = threadIdx.x; e < 32 * kRow; e += blockDim.x) {
+    const int p = e % kRow, s0 = 8 * (e / kRow);
+    const uint16_t *src = cdf + chan_of(p) * 256 + s0;
+    const uint4 v = *reinterpret_cast<const uint4 *>(src);
+    const uint32_t nx = s0 + 8 < 256 ? uint32_t(src[8]) : kM;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    bool bad = s0 == 0 && (w[0] & 0xFFFFu) != 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const uint32_t c0 = (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+      const uint32_t c1 = q < 7 ? (w[(q + 1) >> 1] >> (16 * ((q + 1) & 1))) & 0xFFFFu : nx;
+      bad |= c1 <= c0;
+      cdfc[(s0 + q) * kRow + p] = uint16_t(c0);
+      if (s0 + q == 255) cdfc[256 * kRow + p] = uint16_t(c0);  // row 256 = cdf_255: f_255 reads as 0
     }
-    for (uint32_t b = (c0 + kBucketSlots - 1) >> kBucketShift; b <= ((c1 - 1) >> kBucketShift) && c1 > c0; b++) {
-      const uint32_t bnd = min(c1 - kBucketSlots * b, kBucketSlots) - 1;  // last slot of s in bucket b
-      lut16[b * (kLpt * T) + col] = uint16_t((s << 8) | (255 - bnd));
+    if (bad) s_bad = 1;
+  }
+  for (int p = threadIdx.x; p < kRow; p += blockDim.x) cdfc[257 * kRow + p] = 0;  // pad row
+  __syncthreads();
+  // bucket entries: a thread walks 64 buckets of the two positions of one
+  // 32-bit word, carrying the current symbol from bucket to bucket
+  for (int e = threadIdx.x; e < 8 * 2 * T; e += blockDim.x) {
+    const int wd = e % (2 * T), b0 = 64 * (e / (2 * T));
+#pragma unroll
+    for (int hpos = 0; hpos < 2; hpos++) {
+      const uint16_t *colp = cdfc + 2 * wd + hpos;
+      // largest s with cdf_s <= 128 b0 (cdf_0 = 0)
+      uint32_t s = 0;
+#pragma unroll
+      for (uint32_t stp = 128; stp; stp >>= 1)
+        if (s + stp <= 255 && colp[(s + stp) * kRow] <= kBucketSlots * b0) s += stp;
+      for (int bb = 0; bb < 64; bb++) {
+        const uint32_t slot0 = kBucketSlots * (b0 + bb);
+        while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
+        // the neighbouring pair (sa, sa + 1) holding most slots of the bucket
+        uint32_t sa = s;
+        {
+          uint32_t t = s, beg = slot0, prev = 0, best = 0;
+          for (;;) {
+            const uint32_t nt = t < 255 ? uint32_t(colp[(t + 1) * kRow]) : kM;
+            const uint32_t cnt = min(nt, slot0 + kBucketSlots) - beg;  // in-bucket slots of t
+            if (t > s && prev + cnt > best) {
+              best = prev + cnt;
+              sa = t - 1;
+            }
+            if (t == 255 || nt >= slot0 + kBucketSlots) break;
+            prev = cnt;
+            beg = nt;
+            t++;
+          }
+        }
+        const uint32_t nxt = sa < 255 ? uint32_t(colp[(sa + 1) * kRow]) : kM;
+        const uint32_t bnd = min(nxt - slot0, kBucketSlots) - 1;  // last slot of sa in the bucket
+        const uint32_t v = (sa << 8) | (255 - bnd);
+        if (hpos == 0) lut16[(b0 + bb) * kRow + 2 * wd] = uint16_t(v);
+        else lut16[(b0 + bb) * kRow + 2 * wd + 1] = uint16_t(v);
+      }
     }
   }
   __syncthreads();
@@ -239,10 +290,11 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
       orow += lo.d;
       const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
       for (int tt = 0; tt < nt; tt++, orow += lo.d) {
-        // ---- symbol search.  The bucket entry holds the first symbol s0 of
-        // bucket slot>>8 and the last in-bucket offset of its range, so one
-        // compare picks s0 or s0+1; lanes whose bucket holds 3+ symbols
-        // (distribution tails) are marked slow and resolved below.
+        // ---- symbol search.  The bucket entry of slot >> 7 holds a symbol
+        // sa and the last in-bucket offset of sa's range, so one carry picks
+        // sa or sa + 1.  A lane whose slot falls outside that pair (buckets
+        // holding 3+ symbols, the distribution tails) or whose symbol is the
+        // escape (its frequency reads as 0) is marked slow and resolved below.
         uint32_t sy[4], ff[4], rr[4];
         uint32_t slow = 0;
 #pragma unroll
@@ -254,14 +306,16 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
           const uint32_t c0 = ct[sj * (kLpt * T) + cj];
           const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
-          ff[j] = (c1 - c0) & 0xFFFFu;
-          rr[j] = (x[j] & 0xFFFFu) - c0;
+          ff[j] = c1 - c0;
+          rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
           sy[j] = sj;
           slow |= (rr[j] >= ff[j]) ? (1u << j) : 0u;
         }
-        // A bucket holding three or more symbols (the distribution tails,
-        // about 1% of lanes): binary search between the chosen symbol and the
-        // first symbol of the next bucket, in the lane's own table column.
+        // Slow lanes (well under 1%): a binary search in the lane's own table
+        // column, between the previous bucket's pair and the chosen pair when
+        // the slot is below it, else between the pair and the next bucket's
+        // pair; symbol 255 is the escape, whose raw value follows in the words.
+        uint32_t escm = 0;
         if (slow) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
@@ -269,27 +323,35 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
               const int cj = (j >> 1) * T * 2 + (j & 1);
               const uint32_t slot = x[j] & 0xFFFFu;
               const uint32_t b = slot >> kBucketShift;
-              uint32_t lo = sy[j] + 1;  // cdf_lo <= slot is known
-              uint32_t hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
-              while (lo < hi) {
-                const uint32_t mid = (lo + hi + 1) >> 1;
-                if (ct[mid * (kLpt * T) + cj] <= slot) lo = mid;
-                else hi = mid - 1;
+              uint32_t lo = sy[j], hi = lo;
+              if (rr[j] > 0xFFFFu) {  // below the pair: down to the previous bucket's pair
+                hi = lo - 1;
+                lo = b > 0 ? (lt[(b - 1) * (kLpt * T) + cj] >> 8) : 0u;
+              } else if (lo < 255) {  // above the pair (255: the escape symbol, already found)
+                lo += 1;  // cdf_lo <= slot is known
+                hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
+              }
+              {
+                while (lo < hi) {
+                  const uint32_t mid = (lo + hi + 1) >> 1;
+                  if (ct[mid * (kLpt * T) + cj] <= slot) lo = mid;
+                  else hi = mid - 1;
+                }
               }
               const uint32_t c0 = ct[lo * (kLpt * T) + cj];
-              const uint32_t c1 = ct[(lo + 1) * (kLpt * T) + cj];
+              const uint32_t c1 = lo < 255 ? uint32_t(ct[(lo + 1) * (kLpt * T) + cj]) : kM;
               sy[j] = lo;
-              ff[j] = (c1 - c0) & 0xFFFFu;
+              ff[j] = c1 - c0;
               rr[j] = slot - c0;
+              escm |= lo == uint32_t(kEsc) ? (1u << j) : 0u;
             }
           }
         }
-        uint32_t needm = 0, escm = 0;
+        uint32_t needm = 0;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           x[j] = ff[j] * (x[j] >> 16) + rr[j];
           needm |= (x[j] < kRansL) ? (1u << j) : 0u;
-          escm |= (sy[j] == kEsc) ? (1u << j) : 0u;
         }
         const int cntw = __popc(needm) + 2 * __popc(escm);
         // ---- word positions: team-wide exclusive scan of the word counts
