@@ -7,10 +7,13 @@
 //
 //   k_encode          one CTA per (level, head); a team of d/4 threads
 //                     encodes one chunk's stream, 4 lanes per thread, in
-//                     reverse token order.  Per token the team orders its
-//                     words with a shuffle scan (lanes descending) and writes
-//                     them backwards into the stream's scratch slot, so the
-//                     scratch ends up in decode order.
+//                     reverse token order, the next rows loaded while the
+//                     current ones are coded.  Per token the team orders its
+//                     words with a shuffle scan (lanes descending) and stages
+//                     them in a shared-memory ring; each full block of 256
+//                     words goes backwards into the stream's scratch slot
+//                     with 16-byte stores, so the scratch ends up in decode
+//                     order.
 //   k_scan_chunks     per chunk: exclusive scan of the padded stream sizes.
 //   k_scan_total      chunk offsets and the container size.
 //   k_compact_fixed   container header, chunk headers, scales, anchors and
@@ -32,19 +35,18 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 // One rANS encode step after renormalisation (x < f * 2^16):
 //   x' = floor(x / f) * 2^16 + (x mod f) + cdf.
-// The quotient (< 2^16) is estimated in fp32 (relative error < 2^-21, so
-// the estimate is off by at most one) and corrected exactly.
+// The quotient (< 2^16) is estimated in fp32 as x * rcp(f) - 1/4: the
+// estimate's error is below 2^-6, so after the offset it lies strictly
+// between x/f - 0.27 and x/f - 0.23 and truncates to the quotient or one
+// less; one exact correction step finishes it.
 __device__ __forceinline__ uint32_t rans_put(uint32_t x, uint32_t f, uint32_t c) {
-  uint32_t q = __float2uint_rz(__fmul_rz(__uint2float_rz(x), rcp_approx(float(f))));
-  int32_t r = int32_t(x - q * f);
-  if (r < 0) {
-    q -= 1;
-    r += int32_t(f);
-  } else if (r >= int32_t(f)) {
+  uint32_t q = __float2uint_rz(__fmaf_rz(__uint2float_rz(x), rcp_approx(float(f)), -0.25f));
+  uint32_t r = x - q * f;
+  if (r >= f) {
     q += 1;
-    r -= int32_t(f);
+    r -= f;
   }
-  return (q << 16) + uint32_t(r) + c;
+  return (q << 16) + r + c;
 }
 
 template <int T>
@@ -55,12 +57,27 @@ __device__ __forceinline__ uint32_t team_mask() {
 
 constexpr int kLpt = kLanesPerThread;
 
+// Words staged per team before they go to the scratch slot.  A token adds at
+// most 12 words per thread (384 per team), and at most 255 wait in a partly
+// filled block, so 1024 slots never overwrite a word not yet stored.
+constexpr uint32_t kWordRing = 1024;
+
+// Block blk of 256 words (encoder order 256 blk ..) from the ring to the
+// scratch slot, whose words [cap - 256 (blk + 1), cap - 256 blk) it fills,
+// 16 bytes per store; units below u0 are skipped.
+__device__ __forceinline__ void flush_block(const uint16_t *ring, uint16_t *wout, int64_t cap, uint32_t blk,
+                                            uint32_t u0, int i, int T) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(ring + (kWordRing - 256) - 256 * (blk & 3));
+  uint4 *dst = reinterpret_cast<uint4 *>(wout + cap - 256 * (int64_t(blk) + 1));
+  for (uint32_t u = u0 + i; u < 32; u += T) dst[u] = src[u];
+}
+
 // ---------------------------------------------------------------- k_encode
 template <int T>
 __global__ void __launch_bounds__(max_threads<T>())
 k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv,
          uint8_t *ws) {
-  extern __shared__ __align__(16) uint32_t etab[];  // [256][4][T] : cdf | f << 16
+  extern __shared__ __align__(16) uint32_t etab[];  // [256][4][T] : cdf | f << 16, then the word rings
   const int lv = blockIdx.x, si = blockIdx.y;
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
   const int32_t *counts = reinterpret_cast<const int32_t *>(ws + w.levels);
@@ -80,6 +97,7 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
   __syncthreads();
 
   const int team = threadIdx.x / T, i = threadIdx.x % T, nteams = blockDim.x / T;
+  uint16_t *ring = reinterpret_cast<uint16_t *>(etab + 256 * lo.d) + team * kWordRing;
   const uint32_t tm = team_mask<T>();
   const float4 rc4 = *reinterpret_cast<const float4 *>(
       reinterpret_cast<const float *>(tables + lo.tb_recip) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
@@ -102,74 +120,109 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
     uint32_t x[4] = {kRansL, kRansL, kRansL, kRansL};
     int64_t E = 0;      // words emitted so far (encoder order)
     uint32_t nesc = 0;
-    bool bad = false, overflow = false;
-    for (int g = ng - 1; g >= 0 && !overflow; g--) {
-      const uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
-      float ah[4];
+    uint32_t badm = 0;  // bit 15 of a half set: an all-ones exponent was seen
+    bool overflow = false;
+    // tokens in reverse order, kAhead rows per batch, the next batch loaded
+    // while this one is encoded; anchor rows are loaded and skipped
+    constexpr int kAhead = 2;
+    int t = ntok - 1;
+    int g = t / lo.G, r = t - g * lo.G;  // group of t and t's place in it
+    uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
+    uint32_t a4n = g > 0 ? *reinterpret_cast<const uint32_t *>(anc + uint64_t(g - 1) * lo.d) : 0u;
+    float ah[4];
 #pragma unroll
-      for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
-      const int tend = min(g * lo.G + lo.G, ntok);
-      // delta tokens of the group in reverse, kAhead rows loaded at a time
-      constexpr int kAhead = 4;
-      for (int tb = tend - 1; tb > g * lo.G && !overflow; tb -= kAhead) {
-        const int nb = min(kAhead, tb - g * lo.G);
-        uint2 rows[kAhead];
+    for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
+    uint2 cur[kAhead], nxt[kAhead];
 #pragma unroll
-        for (int u = 0; u < kAhead; u++)
-          if (u < nb) rows[u] = __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tb - u) * lo.d));
+    for (int u = 0; u < kAhead; u++)
+      cur[u] = t - u >= 0 ? __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(t - u) * lo.d)) : make_uint2(0, 0);
+    while (t >= 1 && !overflow) {
 #pragma unroll
-        for (int u = 0; u < kAhead; u++) {
-          if (u >= nb || overflow) break;
-          const uint2 raw = rows[u];
-          const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-          uint32_t word[4], qv[4];
-          bool esc[4], ren[4];
-          int cntw = 0;
-#pragma unroll
-          for (int j = 3; j >= 0; j--) {
-            if (((hw[j] >> 10) & 31u) == 31u) bad = true;
-            const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
-            const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
-            esc[j] = !(q >= -R && q <= R);
-            const int sym = esc[j] ? kEsc : q + 127;
-            const uint32_t e = etab[(sym * kLpt + j) * T + i];
-            const uint32_t f = e >> 16, c = e & 0xFFFFu;
-            ren[j] = x[j] >= (f << 16);
-            word[j] = x[j] & 0xFFFFu;
-            const uint32_t xr = ren[j] ? (x[j] >> 16) : x[j];
-            x[j] = rans_put(xr, f, c);
-            qv[j] = uint32_t(q);
-            cntw += (esc[j] ? 2 : 0) + (ren[j] ? 1 : 0);
-          }
-          // emission order: lanes descending, i.e. threads descending
-          int suf = cntw;
-#pragma unroll
-          for (int o = 1; o < T; o <<= 1) {
-            const int v = __shfl_down_sync(tm, suf, o, T);
-            if (i + o < T) suf += v;
-          }
-          const int tot = __shfl_sync(tm, suf, 0, T);
-          if (E + tot > cap) {
-            overflow = true;
-            break;
-          }
-          int64_t e = E + (suf - cntw);
-#pragma unroll
-          for (int j = 3; j >= 0; j--) {
-            if (esc[j]) {
-              wout[cap - 1 - e] = uint16_t(qv[j] >> 16);
-              wout[cap - 2 - e] = uint16_t(qv[j] & 0xFFFFu);
-              e += 2;
-              nesc++;
-            }
-            if (ren[j]) {
-              wout[cap - 1 - e] = uint16_t(word[j]);
-              e += 1;
-            }
-          }
-          E += tot;
-        }
+      for (int u = 0; u < kAhead; u++) {
+        const int tn = t - kAhead - u;
+        nxt[u] = tn >= 0 ? __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tn) * lo.d)) : make_uint2(0, 0);
       }
+#pragma unroll
+      for (int u = 0; u < kAhead; u++) {
+        if (t < 1 || overflow) break;
+        if (r == 0) {  // the anchor token of group g: on to group g - 1
+          g--;
+          r = lo.G - 1;
+          a4 = a4n;
+          if (g > 0) a4n = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g - 1) * lo.d);
+#pragma unroll
+          for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
+          t--;
+          continue;
+        }
+        const uint2 raw = cur[u];
+        badm |= ((raw.x & 0x7C007C00u) + 0x04000400u) | ((raw.y & 0x7C007C00u) + 0x04000400u);
+        const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+        uint32_t word[4], qv[4];
+        bool esc[4], ren[4];
+        int cntw = 0;
+#pragma unroll
+        for (int j = 3; j >= 0; j--) {
+          const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
+          const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
+          esc[j] = !(q >= -R && q <= R);
+          const int sym = esc[j] ? kEsc : q + 127;
+          const uint32_t e = etab[(sym * kLpt + j) * T + i];
+          const uint32_t f = e >> 16, c = e & 0xFFFFu;
+          ren[j] = x[j] >= (f << 16);
+          word[j] = x[j] & 0xFFFFu;
+          const uint32_t xr = ren[j] ? (x[j] >> 16) : x[j];
+          x[j] = rans_put(xr, f, c);
+          qv[j] = uint32_t(q);
+          cntw += (esc[j] ? 2 : 0) + (ren[j] ? 1 : 0);
+        }
+        // emission order: lanes descending, i.e. threads descending
+        int suf = cntw;
+#pragma unroll
+        for (int o = 1; o < T; o <<= 1) {
+          const int v = __shfl_down_sync(tm, suf, o, T);
+          if (i + o < T) suf += v;
+        }
+        const int tot = __shfl_sync(tm, suf, 0, T);
+        if (E + tot > cap) {
+          overflow = true;
+          break;
+        }
+        // word e of the stream (encoder order) goes to ring slot ~e mod the
+        // ring size, so a block of 256 words sits in the ring in the order it
+        // takes at the end of the scratch slot (which is filled backwards)
+        uint32_t e = uint32_t(E) + uint32_t(suf - cntw);
+#pragma unroll
+        for (int j = 3; j >= 0; j--) {
+          if (esc[j]) {
+            ring[~e & (kWordRing - 1)] = uint16_t(qv[j] >> 16);
+            ring[~(e + 1) & (kWordRing - 1)] = uint16_t(qv[j] & 0xFFFFu);
+            e += 2;
+            nesc++;
+          }
+          if (ren[j]) {
+            ring[~e & (kWordRing - 1)] = uint16_t(word[j]);
+            e += 1;
+          }
+        }
+        const uint32_t e0 = uint32_t(E), e1 = e0 + uint32_t(tot);
+        if ((e1 >> 8) != (e0 >> 8)) {  // blocks completed: 16-byte stores into the slot
+          __syncwarp(tm);
+          for (uint32_t blk = e0 >> 8; blk < (e1 >> 8); blk++) flush_block(ring, wout, cap, blk, 0, i, T);
+          __syncwarp(tm);  // the block's reads are done before its slots take new words
+        }
+        E += tot;
+        t--;
+        r--;
+      }
+#pragma unroll
+      for (int u = 0; u < kAhead; u++) cur[u] = nxt[u];
+    }
+    const bool bad = (badm & 0x80008000u) != 0;
+    if (!overflow && (E & 255)) {  // the last, partial block: only units that hold its words
+      __syncwarp(tm);
+      const uint32_t blk = uint32_t(E) >> 8;
+      flush_block(ring, wout, cap, blk, (256 * (blk + 1) - uint32_t(E)) / 8, i, T);
     }
     if (bad) atomicOr(status, kStNonfinite);
     if (overflow) {
@@ -391,11 +444,11 @@ k_compact_stream(Layout lo, EncWs w, const uint8_t *__restrict__ ws, uint8_t *__
 template <int T>
 cudaError_t launch_encode_t(const Layout &lo, const EncWs &w, const uint8_t *tables,
                             const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
-  const size_t smem = size_t(256) * lo.d * 4;
+  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
+  const size_t smem = size_t(256) * lo.d * 4 + size_t(teams) * kWordRing * 2;
   cudaError_t e = cudaFuncSetAttribute(k_encode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
-  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
   k_encode<T><<<grid, teams * T, smem, st>>>(lo, w, tables, kv, ws);
   return cudaGetLastError();
 }
