@@ -271,6 +271,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     load_half(kHalf);
     uint32_t rbase = 0;  // the ring holds words [rbase, rbase + kRing)
     uint32_t ready = 0;  // words [rbase, ready) have landed and are visible to the team
+    uint32_t lim = 0;    // p + tot <= lim: no check, refill or wait needed
     const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
     const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
@@ -296,7 +297,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         // holding 3+ symbols, the distribution tails) or whose symbol is the
         // escape (its frequency reads as 0) is marked slow and resolved below.
         uint32_t sy[4], ff[4], rr[4];
-        uint32_t slow = 0;
+        bool sl[4];
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           const int cj = (j >> 1) * T * 2 + (j & 1);
@@ -309,17 +310,17 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           ff[j] = c1 - c0;
           rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
           sy[j] = sj;
-          slow |= (rr[j] >= ff[j]) ? (1u << j) : 0u;
+          sl[j] = rr[j] >= ff[j];
         }
         // Slow lanes (well under 1%): a binary search in the lane's own table
         // column, between the previous bucket's pair and the chosen pair when
         // the slot is below it, else between the pair and the next bucket's
         // pair; symbol 255 is the escape, whose raw value follows in the words.
         uint32_t escm = 0;
-        if (slow) {
+        if (sl[0] | sl[1] | sl[2] | sl[3]) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            if ((slow >> j) & 1u) {
+            if (sl[j]) {
               const int cj = (j >> 1) * T * 2 + (j & 1);
               const uint32_t slot = x[j] & 0xFFFFu;
               const uint32_t b = slot >> kBucketShift;
@@ -362,11 +363,13 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           if (i >= o) incl += v;
         }
         const uint32_t tot = uint32_t(__shfl_sync(tm, incl, T - 1, T));
+        uint32_t pos = p + uint32_t(incl - cntw);
+        bool in_ring = true;
+        if (p + tot > lim) {  // past the words known to be staged, or a refill may be due
         if (p + tot > nw) {
           broken = true;
           break;
         }
-        uint32_t pos = p + uint32_t(incl - cntw);
         // make words [p, p + tot) available in the ring
         if (p >= rbase + kHalf) {
           __syncwarp(tm);  // every thread's reads of the consumed half are done
@@ -375,7 +378,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             rbase += kHalf;
           } while (p >= rbase + kHalf);
         }
-        const bool in_ring = p + tot <= rbase + kRing;
+        in_ring = p + tot <= rbase + kRing;
         if (p + tot > ready) {  // words past what is known to have landed
           if (p + tot <= rbase + kHalf) {
             cp_async_wait_prev();
@@ -385,6 +388,8 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             ready = rbase + kRing;
           }
           __syncwarp(tm);
+        }
+        lim = min(nw, min(ready, rbase + kHalf));
         }
         p += tot;
         float v[4];

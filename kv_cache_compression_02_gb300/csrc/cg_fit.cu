@@ -50,23 +50,30 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 // ---------------------------------------------------------------- k_stats
 // One CTA per head; each thread owns 4 channels (one 8-byte load per token)
 // and a strided subset of the tokens.  An fp16 value is X = M * 2^E (times
-// 2^-24) with M < 2^11, so X^2 = M^2 << 2E is one 32-bit multiply and a
-// shifted add into a 128-bit sum.  Integer sums are order-free, so the
-// reduction order does not matter for the result.
+// 2^-24) with M < 2^11, so X^2 = M^2 << 2E is one 32-bit multiply whose
+// shifted value spans two 32-bit limbs of a 128-bit sum, added with one
+// carry chain.  Integer sums are order-free, so the reduction order does
+// not matter for the result.
 constexpr int kStatsThreads = 512;
 
-__device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint64_t &Qlo, uint64_t &Qhi) {
+__device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint32_t (&q)[4]) {
   const uint32_t e = (h >> 10) & 31u;
   const uint32_t M = e ? ((h & 1023u) | 1024u) : (h & 1023u);
   const uint32_t E = e ? e - 1 : 0;  // X = M << E
   const int64_t X = int64_t(uint64_t(M) << E);
   T += (h & 0x8000u) ? -X : X;
-  const uint32_t m2 = M * M;  // < 2^22
-  const uint32_t sh = 2 * E;  // 0..58
-  const uint64_t lo = uint64_t(m2) << sh;                         // low 64 bits of m2 << sh
-  const uint32_t hi = sh > 42 ? (m2 >> (64 - sh)) : 0u;           // bits 64.. of m2 << sh
-  Qlo += lo;
-  Qhi += uint64_t(hi) + (Qlo < lo ? 1u : 0u);
+  const uint32_t m2 = M * M;     // < 2^22
+  const uint32_t sh = 2 * E;     // 0..60: m2 << sh lies in limbs sh/32 and sh/32 + 1
+  const uint32_t a = m2 << (sh & 31u);
+  const uint32_t b = __funnelshift_l(m2, 0u, sh & 31u);  // the bits shifted out of a
+  const bool up = sh >= 32;
+  const uint32_t v0 = up ? 0u : a, v1 = up ? a : b, v2 = up ? b : 0u;
+  asm("add.cc.u32 %0, %0, %4;\n\t"
+      "addc.cc.u32 %1, %1, %5;\n\t"
+      "addc.cc.u32 %2, %2, %6;\n\t"
+      "addc.u32 %3, %3, 0;"
+      : "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3])
+      : "r"(v0), "r"(v1), "r"(v2));
 }
 
 __global__ void __launch_bounds__(kStatsThreads, 2)
@@ -80,10 +87,13 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 4 * col;
 
   int64_t T[4];
-  uint64_t Qlo[4], Qhi[4];
+  uint32_t Q[4][4];
 #pragma unroll
-  for (int i = 0; i < 4; i++) { T[i] = 0; Qlo[i] = 0; Qhi[i] = 0; }
-  uint32_t bad = 0;
+  for (int i = 0; i < 4; i++) {
+    T[i] = 0;
+    Q[i][0] = Q[i][1] = Q[i][2] = Q[i][3] = 0;
+  }
+  uint32_t bad = 0;  // bit 15 of a half: an all-ones exponent (Inf or NaN) was seen
   for (int64_t t0 = row; t0 < lo.S; t0 += 4 * int64_t(rows)) {
     uint2 vv[4];
 #pragma unroll
@@ -94,14 +104,12 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const uint32_t hw[4] = {vv[u].x & 0xFFFFu, vv[u].x >> 16, vv[u].y & 0xFFFFu, vv[u].y >> 16};
+      bad |= ((vv[u].x & 0x7C007C00u) + 0x04000400u) | ((vv[u].y & 0x7C007C00u) + 0x04000400u);
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        bad |= (hw[i] & 0x7C00u) == 0x7C00u;
-        acc_moments(hw[i], T[i], Qlo[i], Qhi[i]);  // a non-finite value only spoils a flagged result
-      }
+      for (int i = 0; i < 4; i++) acc_moments(hw[i], T[i], Q[i]);  // a non-finite value only spoils a flagged result
     }
   }
-  if (bad) atomicOr(status, kStNonfinite);
+  if (bad & 0x80008000u) atomicOr(status, kStNonfinite);
 
   int64_t *sT = reinterpret_cast<int64_t *>(smem);          // [rows][d]
   uint64_t *sQl = reinterpret_cast<uint64_t *>(sT + rows * lo.d);
@@ -110,8 +118,8 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   for (int i = 0; i < 4; i++) {
     const int c = 4 * col + i;
     sT[row * lo.d + c] = T[i];
-    sQl[row * lo.d + c] = Qlo[i];
-    sQh[row * lo.d + c] = Qhi[i];
+    sQl[row * lo.d + c] = uint64_t(Q[i][0]) | (uint64_t(Q[i][1]) << 32);
+    sQh[row * lo.d + c] = uint64_t(Q[i][2]) | (uint64_t(Q[i][3]) << 32);
   }
   __syncthreads();
   if (threadIdx.x < lo.d) {
