@@ -9,8 +9,9 @@ resident in HBM when the timed region starts and are larger than L2.
 
 The headline value is decode throughput (fp16 GB/s written by cg_decode);
 encode and fit throughput, the compression ratio, the entropy bound of the
-coded symbols, roofline fractions and an end-to-end figure through host
-buffers are reported beside it.  `--impl reference` times the CPU oracle on
+coded symbols, roofline fractions, an end-to-end figure through host
+buffers, the same decode in layer groups (time to the first group) and into
+a paged (block-table) cache are reported beside it.  `--impl reference` times the CPU oracle on
 a bounded sample of the same workload instead.
 
 Multi-GPU: every rank codes its own copy of the workload (independent
@@ -46,6 +47,7 @@ def parse():
     ap.add_argument("--workload", default="llama3_70b_L80_H8_d128_S32768")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-paged", action="store_true", help="skip the layer-group and paged-cache decode legs")
     ap.add_argument("--layers", type=int, default=0,
                     help="run the same workload with fewer layers (a smaller case for profiling)")
     return ap.parse_args()
@@ -310,6 +312,60 @@ def main():
             e2e_ms.append(a.elapsed_time(b))
     cg.check(cg.cg_read_status(ws_dec), "decode (e2e)")
 
+    # the same decode in layer groups, in execution order: 19 layers (304
+    # CTAs, two full waves) per launch, an event after each group
+    lgroups = None
+    if not args.no_paged:
+        per = 19
+        bounds = [(l0, min(l0 + per, w.L)) for l0 in range(0, w.L, per)]
+        lev = []
+        for i in range(max(args.warmup, 1) + args.steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(bounds) + 1)]
+            evs[0].record(stream)
+            for gi, (l0, l1) in enumerate(bounds):
+                cg.check(cg.cg_decode_layers(cfg, tables, out, nbytes, 0, -1, l0, l1, kv_out, ws_dec, stream),
+                         "cg_decode_layers")
+                evs[gi + 1].record(stream)
+            if i >= max(args.warmup, 1):
+                lev.append(evs)
+        torch.cuda.synchronize()
+        cg.check(cg.cg_read_status(ws_dec), "decode (layer groups)")
+        first = statistics.mean(e[0].elapsed_time(e[1]) for e in lev)
+        total = statistics.mean(e[0].elapsed_time(e[-1]) for e in lev)
+        lgroups = {"layers_per_group": per, "groups": len(bounds), "first_group_ms": first, "all_groups_ms": total,
+                   "fp16_gbs": w.fp16_bytes / (total * 1e-3) / 1e9}
+
+    # the same decode into a paged cache: 16-token blocks, shuffled block table
+    paged = None
+    if not args.no_paged:
+        bt = 16
+        n_lblk = -(-w.S // bt)
+        pools = torch.empty((w.L * 2, n_lblk, w.H, bt, w.d), dtype=torch.int16, device=dev)
+        ptrs = torch.tensor([pools.data_ptr() + i * pools.stride(0) * 2 for i in range(w.L * 2)],
+                            dtype=torch.int64, device=dev)
+        table = torch.randperm(n_lblk, generator=torch.Generator().manual_seed(0)).to(torch.int32).to(dev)
+        pev = []
+        for i in range(max(args.warmup, 1) + args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cg.check(cg.cg_decode_paged(cfg, tables, out, nbytes, 0, -1, ptrs, table, bt, n_lblk, ws_dec, stream),
+                     "cg_decode_paged")
+            b.record(stream)
+            if i >= max(args.warmup, 1):
+                pev.append((a, b))
+        torch.cuda.synchronize()
+        cg.check(cg.cg_read_status(ws_dec), "decode (paged)")
+        # spot check: a few logical blocks hold the contiguous decode's rows
+        kvo = kv_out.view(w.L * 2, w.H, w.S, w.d)
+        for lb in (0, n_lblk // 2, n_lblk - 1):
+            t0, t1 = lb * bt, min(w.S, lb * bt + bt)
+            if not torch.equal(pools[:, int(table[lb]), :, : t1 - t0], kvo[:, :, t0:t1]):
+                raise RuntimeError("paged decode differs from the contiguous decode")
+        ms_paged = statistics.mean(a.elapsed_time(b) for a, b in pev)
+        paged = {"ms": ms_paged, "fp16_gbs": w.fp16_bytes / (ms_paged * 1e-3) / 1e9, "block_tokens": bt,
+                 "table": "random permutation of the sequence's blocks"}
+        del pools
+
     # aggregate over ranks: max time, summed bytes
     def agg_max(v):
         if world == 1:
@@ -365,6 +421,8 @@ def main():
                             "algorithmic_bytes_per_launch": enc_alg},
         "e2e": {"value": world * fp16 / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": nbytes,
                 "d2h_bytes_per_step": fp16, "what": "pinned-host container -> cg_decode -> pinned-host KV"},
+        "decode_paged": paged,
+        "decode_layer_groups": lgroups,
         "gpu_launches": args.steps * (3 + 6 + 2),
         "clocks": clk,
         "cpu_baseline": cpu,

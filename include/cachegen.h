@@ -62,7 +62,9 @@ extern "C" {
 
 typedef enum {
     CG_OK = 0,
-    CG_ERR_INVALID_ARG = 1, /* bad dims/params/pointer/size (synchronous)   */
+    CG_ERR_INVALID_ARG = 1, /* bad dims/params/pointer/size (synchronous;
+                               also a bad page-table entry found on the
+                               device by cg_decode_paged)                  */
     CG_ERR_NONFINITE = 2,   /* an input element is Inf or NaN              */
     CG_ERR_CAPACITY = 3,    /* output or workspace too small              */
     CG_ERR_CORRUPT = 4,     /* container or tables failed validation      */
@@ -151,6 +153,48 @@ cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *ta
 cg_status cg_decode(const cg_dims *dims, const cg_params *params, const void *tables_dev,
                     const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
                     int32_t chunk_end, void *kv_dev, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* cg_decode restricted to layers [layer_begin, layer_end) (layer_end = -1:
+ * to the last layer): only those layers' tokens of the chosen chunks are
+ * written.  Decoding the layers in groups, in layer order, with an event
+ * recorded after each group lets a consumer start on the first layers
+ * while the later ones are still being decoded (Guide to CacheGen, pillar
+ * 4: layers stream in execution order, layer 0 first, so generation can
+ * begin once layer 0 is decoded).  Values are bit-identical to cg_decode's; arguments
+ * and errors are as for cg_decode, plus CG_ERR_INVALID_ARG for a layer
+ * range outside [0, L]. */
+cg_status cg_decode_layers(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                           const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                           int32_t chunk_end, int32_t layer_begin, int32_t layer_end, void *kv_dev,
+                           void *ws_dev, size_t ws_bytes, void *stream);
+
+/* cg_decode into a paged KV cache instead of the contiguous buffer: the
+ * cache is split into blocks of block_tokens tokens, and a block table maps
+ * each logical block of the sequence to a physical block of a page pool
+ * (the block-table cache layout of paged-attention servers).  The Guide to
+ * CacheGen's deployment notes (integrating with PagedAttention: direct
+ * paged buffer injection) ask the decompressor to write reconstructed
+ * tokens straight into the server's block-table pages; this call does.
+ *   pools_dev:       device array of 2*L pointers; pools_dev[2*l + kv] is
+ *                    the page pool of layer l, K (kv = 0) or V (kv = 1):
+ *                    fp16 [n_blocks][H][block_tokens][d], 16-byte aligned.
+ *   block_table_dev: device int32 array of ceil(S / block_tokens) entries;
+ *                    token t of the sequence goes to row t % block_tokens
+ *                    of block block_table_dev[t / block_tokens], which must
+ *                    lie in [0, n_blocks).  The same table serves every
+ *                    layer and K/V; distinct tokens must map to distinct
+ *                    rows (the library does not check this).
+ *   block_tokens, n_blocks: both >= 1.
+ * Everything else (chunk range, workspace, errors) is as for cg_decode:
+ * only the chosen chunks' tokens are written, every value is bit-identical
+ * to cg_decode's.  A block id out of range, or a null or misaligned pool
+ * pointer, is found on the device: those rows are not written and the
+ * status reads CG_ERR_INVALID_ARG (after CG_ERR_CORRUPT, which wins). */
+cg_status cg_decode_paged(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                          const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                          int32_t chunk_end, void *const *pools_dev, const int32_t *block_table_dev,
+                          int32_t block_tokens, int32_t n_blocks, void *ws_dev, size_t ws_bytes,
+                          void *stream);
 
 /* cg_decode without a workspace argument, for callers that cannot
  * allocate device memory: code running while a CUDA graph is captured,

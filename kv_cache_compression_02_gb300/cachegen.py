@@ -61,6 +61,10 @@ def lib() -> ctypes.CDLL:
             "cg_read_status": (ctypes.c_int, [P]),
             "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                  P, P, ctypes.POINTER(ctypes.c_void_p)]),
+            "cg_decode_layers": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_int32, P, P, S, P]),
+            "cg_decode_paged": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                               P, P, ctypes.c_int32, ctypes.c_int32, P, S, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -161,6 +165,24 @@ def cg_decode_noalloc(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: 
                                  int(nbytes), int(chunk_begin), int(chunk_end), _ptr(kv), _stream(stream),
                                  ctypes.byref(addr))
     return rc, addr.value
+
+
+def cg_decode_layers(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: int, chunk_end: int,
+                     layer_begin: int, layer_end: int, kv, ws, stream=None) -> int:
+    return lib().cg_decode_layers(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(tables), _ptr(bitstream),
+                                  int(nbytes), int(chunk_begin), int(chunk_end), int(layer_begin), int(layer_end),
+                                  _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def cg_decode_paged(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: int, chunk_end: int, pools,
+                    block_table, block_tokens: int, n_blocks: int, ws, stream=None) -> int:
+    """cg_decode into a paged cache.  pools: device int64 tensor of the 2*L
+    page-pool addresses ([n_blocks][H][block_tokens][d] fp16 each);
+    block_table: device int32 tensor of ceil(S / block_tokens) block ids."""
+    return lib().cg_decode_paged(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(tables), _ptr(bitstream),
+                                 int(nbytes), int(chunk_begin), int(chunk_end), _ptr(pools), _ptr(block_table),
+                                 int(block_tokens), int(n_blocks), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream(stream))
 
 
 def cg_read_status(ws) -> int:

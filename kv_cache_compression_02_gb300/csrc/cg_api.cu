@@ -32,6 +32,33 @@ cg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CG_OK : CG_ERR_
 
 }  // namespace
 
+// The decode entry points: chunks [k0, k1) of layers [l0, l1) (l1 = -1: to
+// the last layer) into kv_dev, or into the paged cache *po when po is set.
+static cg_status decode_common(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                        const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                        int32_t chunk_end, int32_t l0, int32_t l1, void *kv_dev, const PagedOut *po,
+                        void *ws_dev, size_t ws_bytes, void *stream) {
+  Layout lo;
+  if (!layout_of(dims, params, lo) || !tables_dev || !bitstream_dev || (!po && !kv_dev) || !ws_dev)
+    return CG_ERR_INVALID_ARG;
+  if (!aligned(tables_dev, 16) || !aligned(bitstream_dev, 16) || !aligned(kv_dev, 16) ||
+      !aligned(ws_dev, 256))
+    return CG_ERR_INVALID_ARG;
+  if (chunk_end < 0) chunk_end = lo.n_chunks;
+  if (chunk_begin < 0 || chunk_begin > chunk_end || chunk_end > lo.n_chunks) return CG_ERR_INVALID_ARG;
+  if (l1 < 0) l1 = lo.L;
+  if (l0 < 0 || l0 > l1 || l1 > lo.L) return CG_ERR_INVALID_ARG;
+  const DecWs w = dec_ws(lo);
+  if (ws_bytes < w.bytes || bitstream_bytes < lo.hdr_bytes) return CG_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(ws_dev);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e == cudaSuccess && chunk_begin < chunk_end && l0 < l1)
+    e = launch_decode(lo, static_cast<const uint8_t *>(tables_dev), static_cast<const uint8_t *>(bitstream_dev),
+                      bitstream_bytes, chunk_begin, chunk_end, static_cast<uint16_t *>(kv_dev), ws, st, po, l0, l1);
+  return cuda_status(e);
+}
+
 extern "C" {
 
 int32_t cg_version(void) { return 1; }
@@ -159,23 +186,29 @@ cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *ta
 cg_status cg_decode(const cg_dims *dims, const cg_params *params, const void *tables_dev,
                     const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
                     int32_t chunk_end, void *kv_dev, void *ws_dev, size_t ws_bytes, void *stream) {
-  Layout lo;
-  if (!layout_of(dims, params, lo) || !tables_dev || !bitstream_dev || !kv_dev || !ws_dev)
+  return decode_common(dims, params, tables_dev, bitstream_dev, bitstream_bytes, chunk_begin, chunk_end, 0, -1,
+                       kv_dev, nullptr, ws_dev, ws_bytes, stream);
+}
+
+cg_status cg_decode_layers(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                           const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                           int32_t chunk_end, int32_t layer_begin, int32_t layer_end, void *kv_dev,
+                           void *ws_dev, size_t ws_bytes, void *stream) {
+  return decode_common(dims, params, tables_dev, bitstream_dev, bitstream_bytes, chunk_begin, chunk_end,
+                       layer_begin, layer_end, kv_dev, nullptr, ws_dev, ws_bytes, stream);
+}
+
+cg_status cg_decode_paged(const cg_dims *dims, const cg_params *params, const void *tables_dev,
+                          const void *bitstream_dev, uint64_t bitstream_bytes, int32_t chunk_begin,
+                          int32_t chunk_end, void *const *pools_dev, const int32_t *block_table_dev,
+                          int32_t block_tokens, int32_t n_blocks, void *ws_dev, size_t ws_bytes,
+                          void *stream) {
+  if (!pools_dev || !block_table_dev || block_tokens < 1 || n_blocks < 1 || !aligned(pools_dev, 8) ||
+      !aligned(block_table_dev, 4))
     return CG_ERR_INVALID_ARG;
-  if (!aligned(tables_dev, 16) || !aligned(bitstream_dev, 16) || !aligned(kv_dev, 16) ||
-      !aligned(ws_dev, 256))
-    return CG_ERR_INVALID_ARG;
-  if (chunk_end < 0) chunk_end = lo.n_chunks;
-  if (chunk_begin < 0 || chunk_begin > chunk_end || chunk_end > lo.n_chunks) return CG_ERR_INVALID_ARG;
-  const DecWs w = dec_ws(lo);
-  if (ws_bytes < w.bytes || bitstream_bytes < lo.hdr_bytes) return CG_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t *ws = static_cast<uint8_t *>(ws_dev);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
-  if (e == cudaSuccess && chunk_begin < chunk_end)
-    e = launch_decode(lo, static_cast<const uint8_t *>(tables_dev), static_cast<const uint8_t *>(bitstream_dev),
-                      bitstream_bytes, chunk_begin, chunk_end, static_cast<uint16_t *>(kv_dev), ws, st);
-  return cuda_status(e);
+  const PagedOut po{reinterpret_cast<uint16_t *const *>(pools_dev), block_table_dev, block_tokens, n_blocks};
+  return decode_common(dims, params, tables_dev, bitstream_dev, bitstream_bytes, chunk_begin, chunk_end, 0, -1,
+                       nullptr, &po, ws_dev, ws_bytes, stream);
 }
 
 cg_status cg_read_status(const void *ws_dev) {
@@ -186,6 +219,7 @@ cg_status cg_read_status(const void *ws_dev) {
   if (bits & kStNonfinite) return CG_ERR_NONFINITE;
   if (bits & kStCapacity) return CG_ERR_CAPACITY;
   if (bits & kStTimeout) return CG_ERR_TIMEOUT;
+  if (bits & kStBadArg) return CG_ERR_INVALID_ARG;
   return CG_OK;
 }
 

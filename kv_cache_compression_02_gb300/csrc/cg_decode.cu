@@ -110,6 +110,15 @@ __device__ __forceinline__ uint32_t team_mask() {
   return T == 32 ? 0xffffffffu : (((1u << T) - 1u) << (lane & ~(T - 1)));
 }
 
+// Row tib of physical block b in a paged cache, at thread i's lanes; ok is
+// false (and the row must not be written) when the block id is out of
+// range or the pool pointer is null or misaligned.
+__device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *pool, int32_t b, int tib,
+                                               int h, const Layout &lo, int i, bool &ok) {
+  ok = b >= 0 && b < po.n_blocks && pool != nullptr && (reinterpret_cast<uintptr_t>(pool) & 15) == 0;
+  return pool + ((uint64_t(ok ? b : 0) * lo.H + h) * po.bt + tib) * lo.d + kLpt * i;
+}
+
 // ---------------------------------------------------------------- decode
 // Shared memory per CTA (d lanes, T = d/4 threads per team), 217 KB at d=128
 // with 22 teams:
@@ -123,10 +132,11 @@ __device__ __forceinline__ uint32_t team_mask() {
 // Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
 // access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
-template <int T>
+// PAGED: token rows go to the paged cache po instead of kv.
+template <int T, bool PAGED>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
-         uint16_t *__restrict__ kv, uint8_t *ws) {
+         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
   extern __shared__ __align__(16) uint32_t smem[];
   uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [kBuckets][2][T][2]
   uint16_t *cdfc = lut16 + kBuckets * kLpt * T;                      // [kCdfRows][2][T][2]
@@ -134,6 +144,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
+  if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
   if (cnt == 0) return;
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
@@ -275,11 +286,45 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
     const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
-    uint16_t *out = kv + (uint64_t(si) * lo.S + uint64_t(k) * lo.C) * lo.d + kLpt * i;
     uint32_t p = 0, nesc = 0;
     bool broken = false;
 
-    uint16_t *orow = out;
+    // output row of the team's current token
+    uint16_t *orow;
+    bool row_ok = true, bad_row = false;
+    [[maybe_unused]] uint16_t *pool = nullptr;
+    [[maybe_unused]] int64_t lblk = 0, n_lblk = 0;
+    [[maybe_unused]] int tib = 0, tl = 0;
+    [[maybe_unused]] int32_t bnext = 0;  // block id of logical block lblk + 1, loaded a block ahead
+    if constexpr (PAGED) {
+      pool = po.pools[l * 2 + kvi];
+      const int64_t t0 = int64_t(k) * lo.C;
+      n_lblk = (lo.S + po.bt - 1) / po.bt;
+      lblk = t0 / po.bt;
+      tib = int(t0 - lblk * po.bt);
+      orow = paged_row(po, pool, po.table[lblk], tib, h, lo, i, row_ok);
+      if (lblk + 1 < n_lblk) bnext = po.table[lblk + 1];
+    } else {
+      orow = kv + (uint64_t(si) * lo.S + uint64_t(k) * lo.C) * lo.d + kLpt * i;
+    }
+    auto next_row = [&]() {
+      if constexpr (PAGED) {
+        bad_row |= !row_ok;
+        ++tl;
+        if (++tib == po.bt) {  // next block, if the chunk has another token
+          tib = 0;
+          ++lblk;
+          if (tl < ntok) {
+            orow = paged_row(po, pool, bnext, 0, h, lo, i, row_ok);
+            if (lblk + 1 < n_lblk) bnext = po.table[lblk + 1];
+          }
+        } else {
+          orow += lo.d;
+        }
+      } else {
+        orow += lo.d;
+      }
+    };
     uint32_t a4n = *reinterpret_cast<const uint32_t *>(anc);  // next group's anchors, loaded ahead
     for (int g = 0; g < ng && !broken; g++) {
       const uint32_t a4 = a4n;
@@ -287,10 +332,11 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
       float ah[4];
 #pragma unroll
       for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
-      *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(ah[0], ah[1]), pack_f16x2(ah[2], ah[3]));
-      orow += lo.d;
+      if (!PAGED || row_ok)
+        *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(ah[0], ah[1]), pack_f16x2(ah[2], ah[3]));
+      next_row();
       const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
-      for (int tt = 0; tt < nt; tt++, orow += lo.d) {
+      for (int tt = 0; tt < nt; tt++, next_row()) {
         // ---- symbol search.  The bucket entry of slot >> 7 holds a symbol
         // sa and the last in-bucket offset of sa's range, so one carry picks
         // sa or sa + 1.  A lane whose slot falls outside that pair (buckets
@@ -447,10 +493,12 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           }
         }
         }
-        *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
+        if (!PAGED || row_ok)
+          *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
       }
     }
     cp_async_wait_all();
+    if (PAGED && bad_row) atomicOr(status, kStBadArg);
 #pragma unroll
     for (int o = T / 2; o; o >>= 1) nesc += __shfl_xor_sync(tm, nesc, o, T);
     const bool lanes_ok = x[0] == kRansL && x[1] == kRansL && x[2] == kRansL && x[3] == kRansL;
@@ -458,34 +506,43 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   }
 }
 
-template <int T>
-cudaError_t launch_decode_t(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
-                            uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
+template <int T, bool PAGED>
+cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
+                             uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po,
+                             int l0, int l1) {
   if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
   const size_t smem = size_t(kBuckets + kCdfRows) * lo.d * 2 + size_t(teams) * kRing * 2;
-  cudaError_t e = cudaFuncSetAttribute(k_decode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = cudaFuncSetAttribute(k_decode<T, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, lo.nstr);
-  k_decode<T><<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws);
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
+  k_decode<T, PAGED><<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
+}
+
+template <int T>
+cudaError_t launch_decode_t(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
+                            uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st, const PagedOut *po,
+                            int l0, int l1) {
+  if (po) return launch_decode_tp<T, true>(lo, tables, buf, kv, ws, teams, st, *po, l0, l1);
+  return launch_decode_tp<T, false>(lo, tables, buf, kv, ws, teams, st, PagedOut{nullptr, nullptr, 1, 0}, l0, l1);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                           uint64_t bytes, int32_t k0, int32_t k1, uint16_t *kv, uint8_t *ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, const PagedOut *po, int32_t l0, int32_t l1) {
   k_decode_index<<<1, 32, 0, st>>>(lo, tables, buf, bytes, k0, k1, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int teams = k1 - k0;
   if (teams < 1) return cudaSuccess;
   switch (lo.d / kLpt) {
-    case 2: return launch_decode_t<2>(lo, tables, buf, kv, ws, teams, st);
-    case 4: return launch_decode_t<4>(lo, tables, buf, kv, ws, teams, st);
-    case 8: return launch_decode_t<8>(lo, tables, buf, kv, ws, teams, st);
-    case 16: return launch_decode_t<16>(lo, tables, buf, kv, ws, teams, st);
-    case 32: return launch_decode_t<32>(lo, tables, buf, kv, ws, teams, st);
+    case 2: return launch_decode_t<2>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+    case 4: return launch_decode_t<4>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+    case 8: return launch_decode_t<8>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+    case 16: return launch_decode_t<16>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+    case 32: return launch_decode_t<32>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -27,8 +27,18 @@ cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, u
                                 uint64_t cap, uint64_t *out_bytes, cudaStream_t st);
 
 // cg_decode.cu
+// A paged KV cache: the pool of layer l, K/V kv is fp16
+// [n_blocks][H][bt][d] at pools[2 l + kv]; token t of the sequence is row
+// t mod bt of block table[t / bt].
+struct PagedOut {
+  uint16_t *const *pools;
+  const int32_t *table;
+  int32_t bt, n_blocks;
+};
+// Decodes chunks [k0, k1) of layers [l0, l1) into the contiguous kv buffer,
+// or into the paged cache po when po is not null (kv is then unused).
 cudaError_t launch_decode(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                           uint64_t bytes, int32_t k0, int32_t k1, uint16_t *kv, uint8_t *ws,
-                          cudaStream_t st);
+                          cudaStream_t st, const PagedOut *po, int32_t l0, int32_t l1);
 
 }  // namespace cg

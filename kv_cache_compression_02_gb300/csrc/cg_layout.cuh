@@ -23,6 +23,7 @@ constexpr uint32_t kStNonfinite = 1u;
 constexpr uint32_t kStCapacity = 2u;
 constexpr uint32_t kStCorrupt = 4u;
 constexpr uint32_t kStTimeout = 8u;
+constexpr uint32_t kStBadArg = 16u;    // an argument read on the device was invalid
 
 __host__ __device__ inline uint64_t pad16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
 __host__ __device__ inline uint64_t pad256(uint64_t v) { return (v + 255) & ~uint64_t(255); }

@@ -84,6 +84,7 @@ extern "C" cg_status cg_decode_noalloc(const cg_dims *dims, const cg_params *par
   if (e == cudaSuccess && chunk_begin < chunk_end)
     e = cg::launch_decode(lo, static_cast<const uint8_t *>(tables_dev),
                           static_cast<const uint8_t *>(bitstream_dev), bitstream_bytes, chunk_begin,
-                          chunk_end, static_cast<uint16_t *>(kv_dev), static_cast<uint8_t *>(ws), st);
+                          chunk_end, static_cast<uint16_t *>(kv_dev), static_cast<uint8_t *>(ws), st,
+                          nullptr, 0, lo.L);
   return e == cudaSuccess ? CG_OK : CG_ERR_CUDA;
 }

@@ -282,6 +282,22 @@ def decode(tables: np.ndarray, container: np.ndarray, k0: int = 0, k1: int | Non
     return rc, out
 
 
+def paged_from_contiguous(kv: np.ndarray, block_table, block_tokens: int, n_blocks: int, fill: int = 0,
+                          tokens=None) -> np.ndarray:
+    """The paged cache that holds kv ([L,2,H,S,d] uint16): pools
+    [L][2][n_blocks][H][block_tokens][d], token t of the sequence at row
+    t % block_tokens of block block_table[t // block_tokens] (the block-table
+    layout the Guide to CacheGen's deployment notes name for paged-attention
+    servers).  Rows no token maps to keep `fill`.  tokens: the token indices
+    to place (default all S)."""
+    L, _, H, S, d = kv.shape
+    pools = np.full((L, 2, n_blocks, H, block_tokens, d), fill, np.uint16)
+    for t in (range(S) if tokens is None else tokens):
+        b = int(block_table[t // block_tokens])
+        pools[:, :, b, :, t % block_tokens, :] = kv[:, :, :, t, :]
+    return pools
+
+
 def decode_stream(cd: Codec, blk, k, step_, cdf, s, anchors, head_out):
     blk = np.ascontiguousarray(blk, np.uint8)
     return lib().orc_decode_stream(_ref(cd.dims()), _p(blk), blk.size, k,

@@ -1,5 +1,6 @@
 """The C ABI: the library loads, exports every function include/cachegen.h
 declares, and its host-only size queries agree with the oracle (no GPU)."""
+import ctypes
 import os
 import re
 
@@ -81,3 +82,12 @@ def test_invalid_arguments(lib):
     cfg = cg.Config(L=1, H=1, d=8, S=10, C=10)
     assert cg.cg_workspace_bytes(cfg, 7) == 0
     assert lib.cg_fit_tables(None, None, None, None, None, 0, None) == cg.CG_ERR_INVALID_ARG
+    # cg_decode_paged: missing pointers or a block size below 1, rejected before any CUDA call
+    ok = cg.Config(L=1, H=1, d=8, S=10, C=10)
+    fake = 1 << 20  # an aligned non-null address that is never dereferenced
+    args = lambda pools, table, bt, nb: (ctypes.byref(ok.dims), ctypes.byref(ok.params), fake, fake, 4096, 0, -1,  # noqa: E731
+                                         pools, table, bt, nb, fake, 1 << 20, None)
+    assert lib.cg_decode_paged(*args(None, fake, 4, 4)) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_decode_paged(*args(fake, None, 4, 4)) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_decode_paged(*args(fake, fake, 0, 4)) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_decode_paged(*args(fake, fake, 4, 0)) == cg.CG_ERR_INVALID_ARG

@@ -464,3 +464,25 @@ def test_hand_worked_interleaved_renorm(orc):
     assert np.array_equal(w.view(np.uint8), g["words"])
     rc, s2, _ = orc.rans_decode(2, st, w, 0, f, cdf)
     assert rc == 0 and np.array_equal(s2, sym)
+
+
+def test_paged_layout_hand_example(orc):
+    """The block-table layout (pools [L][2][n_blocks][H][bt][d]) on a case
+    worked by hand: S=5 tokens in blocks of 2, table [2, 0, 1]."""
+    L, H, S, d = 1, 2, 5, 2
+    kv = np.zeros((L, 2, H, S, d), np.uint16)
+    for k in range(2):
+        for h in range(H):
+            for t in range(S):
+                for j in range(d):
+                    kv[0, k, h, t, j] = 1000 * k + 100 * h + 10 * t + j + 1
+    pools = orc.paged_from_contiguous(kv, [2, 0, 1], 2, 3, fill=7)
+    assert pools.shape == (1, 2, 3, 2, 2, 2)
+    assert pools[0, 1, 0, 1, 1, 0] == 1131    # V, block 0 row 1 = token 3, head 1, j 0
+    assert pools[0, 0, 2, 1, 0, 1] == 102     # K, block 2 row 0 = token 0, head 1, j 1
+    assert pools[0, 0, 1, 0, 0, 0] == 41      # block 1 row 0 = token 4
+    assert (pools[0, :, 1, :, 1, :] == 7).all()  # block 1 row 1: no token (S = 5)
+    # only the listed tokens are placed
+    part = orc.paged_from_contiguous(kv, [2, 0, 1], 2, 3, fill=0, tokens=[2, 3])
+    assert (part[0, :, 2] == 0).all() and (part[0, :, 1] == 0).all()
+    assert part[0, 0, 0, 0, 0, 0] == 21 and part[0, 0, 0, 0, 1, 0] == 31
