@@ -11,7 +11,9 @@ The headline value is decode throughput (fp16 GB/s written by cg_decode);
 encode and fit throughput, the compression ratio, the entropy bound of the
 coded symbols, roofline fractions, an end-to-end figure through host
 buffers, the same decode in layer groups (time to the first group) and into
-a paged (block-table) cache are reported beside it.  `--impl reference` times the CPU oracle on
+a paged (block-table) cache, and a bandwidth-adaptive streaming run (chunk
+levels chosen by the host controller over a simulated link, the planned
+container encoded and decoded on the GPU) are reported beside it.  `--impl reference` times the CPU oracle on
 a bounded sample of the same workload instead.
 
 Multi-GPU: every rank codes its own copy of the workload (independent
@@ -47,7 +49,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_70b_L80_H8_d128_S32768")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--no-paged", action="store_true", help="skip the layer-group and paged-cache decode legs")
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the layer-group, paged-cache and adaptive-streaming legs")
     ap.add_argument("--layers", type=int, default=0,
                     help="run the same workload with fewer layers (a smaller case for profiling)")
     return ap.parse_args()
@@ -366,6 +369,50 @@ def main():
                  "table": "random permutation of the sequence's blocks"}
         del pools
 
+    # bandwidth-adaptive levels over a simulated link: chunk sizes from GPU
+    # encodes at four levels, the host controller picks a level per chunk,
+    # the planned mixed-level container is GPU-encoded and decoded
+    adaptive = None
+    if not args.no_paged:
+        lb4 = (0.05, 0.1, 0.2, 0.4)
+        cfg4 = cg.Config.from_workload(w, level_base=lb4)
+        tb4 = cg.empty_u8(cg.cg_tables_bytes(cfg4))
+        ws4 = cg.empty_u8(max(cg.cg_workspace_bytes(cfg4, op) for op in (cg.CG_OP_FIT, cg.CG_OP_ENCODE,
+                                                                          cg.CG_OP_DECODE)))
+        cg.check(cg.cg_fit_tables(cfg4, kv, tb4, ws4, stream), "cg_fit_tables (4 levels)")
+        nk = w.n_chunks
+        sizes = np.zeros((nk, len(lb4)), np.int64)
+        for lv in range(len(lb4)):
+            cg.check(cg.cg_encode(cfg4, tb4, kv, np.full(nk, lv, np.uint8), out, nbytes_d, ws4, stream),
+                     "cg_encode (one level)")
+            torch.cuda.synchronize()
+            cg.check(cg.cg_read_status(ws4), "encode (one level)")
+            n_lv = int(nbytes_d.item())
+            offs = np.append(out[64:64 + 8 * nk].cpu().numpy().view(np.uint64).astype(np.int64), n_lv)
+            sizes[:, lv] = np.diff(offs)
+            sizes[0, lv] += offs[0]  # the header and chunk index go out with chunk 0
+        nominal, low = 50e9, 12.5e9  # 400 Gb/s, dropping to 100 Gb/s for 25 ms after 20 ms
+        trace = [(0.020, nominal), (0.025, low), (1.0, nominal)]
+        dec = [ms["dec"] * 1e-3 / nk] * nk  # the measured decode, spread evenly over the chunks
+        deadline = 1.1 * sizes[:, 1].sum() / nominal + dec[-1]
+        rc, lv_plan, _, total = cg.cg_plan_levels(sizes, trace, nominal, deadline, dec)
+        cg.check(rc, "cg_plan_levels")
+        fixed = {f"level_{lv}": cg.cg_simulate_stream(sizes, trace, [lv] * nk, dec)[2] for lv in range(len(lb4))}
+        cg.check(cg.cg_encode(cfg4, tb4, kv, lv_plan, out, nbytes_d, ws4, stream), "cg_encode (planned)")
+        torch.cuda.synchronize()
+        n_plan = int(nbytes_d.item())
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cg.check(cg.cg_decode(cfg4, tb4, out, n_plan, 0, -1, kv_out, ws4, stream), "cg_decode (planned)")
+        b.record(stream)
+        torch.cuda.synchronize()
+        cg.check(cg.cg_read_status(ws4), "decode (planned)")
+        adaptive = {"level_base": list(lb4), "link": "400 Gb/s, 100 Gb/s from 20 to 45 ms, then 400 Gb/s",
+                    "deadline_s": deadline, "levels": lv_plan.tolist(), "total_s": total,
+                    "met_deadline": bool(total <= deadline), "fixed_level_total_s": fixed,
+                    "container_bytes": n_plan, "decode_ms": a.elapsed_time(b)}
+        del tb4, ws4
+
     # aggregate over ranks: max time, summed bytes
     def agg_max(v):
         if world == 1:
@@ -423,6 +470,7 @@ def main():
                 "d2h_bytes_per_step": fp16, "what": "pinned-host container -> cg_decode -> pinned-host KV"},
         "decode_paged": paged,
         "decode_layer_groups": lgroups,
+        "adaptive_streaming": adaptive,
         "gpu_launches": args.steps * (3 + 6 + 2),
         "clocks": clk,
         "cpu_baseline": cpu,

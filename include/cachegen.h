@@ -215,6 +215,49 @@ cg_status cg_decode_noalloc(const cg_dims *dims, const cg_params *params, const 
                             int32_t chunk_begin, int32_t chunk_end, void *kv_dev, void *stream,
                             const void **status_ws);
 
+/* ---- Bandwidth-adaptive streaming (host only, no GPU) ------------------
+ * CacheGen adapts each chunk's compression level to the bandwidth the link
+ * offers while the context streams (gptget summary of arXiv 2310.07240,
+ * Methodology; the paper's abstract: raise the compression level when
+ * bandwidth drops, to keep the loading delay low).  The pages give no
+ * formula; the rule below is the plainest one they support.
+ *
+ * A link is a piecewise-constant bandwidth trace: step i lasts `seconds`
+ * at `bytes_per_s`, starting where step i-1 ended (time 0 for step 0); the
+ * last step lasts forever and must have a positive rate. */
+typedef struct {
+    double seconds;
+    double bytes_per_s;
+} cg_link_step;
+
+/* Chooses a level per chunk.  Chunks are sent in order, back to back.
+ * Before chunk k the bandwidth estimate is the throughput observed while
+ * sending chunk k-1 (initial_bytes_per_s for chunk 0); the level is the
+ * first l (levels ordered finest first) with
+ *     sum_{j>=k} chunk_bytes[j][l] / estimate <= deadline_s - now - decode_s[n-1],
+ * else the last (coarsest) level.  Chunk k's decode starts when its bytes
+ * have arrived and chunk k-1's decode has ended and lasts decode_s[k].
+ *   chunk_bytes:  host u64 [n_chunks][n_levels], chunk k's bytes at level l
+ *                 (e.g. from containers encoded at each level).
+ *   decode_s:     host double [n_chunks], >= 0.
+ *   levels_out:   host u8 [n_chunks].
+ *   timeline_out: host double [n_chunks][3] = (send start, arrival,
+ *                 decode end), or NULL.
+ *   total_s_out:  when the last decode ends.
+ * Arithmetic is IEEE double in a fixed order; byte sums are exact.
+ * Errors: CG_ERR_INVALID_ARG (1 <= n_levels <= 8, n_chunks >= 1, finite
+ * non-negative durations and rates, positive initial estimate). */
+cg_status cg_plan_levels(int32_t n_chunks, int32_t n_levels, const uint64_t *chunk_bytes,
+                         const cg_link_step *trace, int32_t n_steps, double initial_bytes_per_s,
+                         double deadline_s, const double *decode_s, uint8_t *levels_out,
+                         double *timeline_out, double *total_s_out);
+
+/* The same link and decode model for given levels (e.g. one fixed level,
+ * for comparison): fills timeline_out (or NULL) and total_s_out. */
+cg_status cg_simulate_stream(int32_t n_chunks, int32_t n_levels, const uint64_t *chunk_bytes,
+                             const cg_link_step *trace, int32_t n_steps, const uint8_t *levels,
+                             const double *decode_s, double *timeline_out, double *total_s_out);
+
 /* Status of the last call that used this workspace (blocking read of the
  * device status word; synchronise the call's stream first). */
 cg_status cg_read_status(const void *ws_dev);

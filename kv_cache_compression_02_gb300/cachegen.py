@@ -61,6 +61,10 @@ def lib() -> ctypes.CDLL:
             "cg_read_status": (ctypes.c_int, [P]),
             "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                  P, P, ctypes.POINTER(ctypes.c_void_p)]),
+            "cg_plan_levels": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_int32, ctypes.c_double,
+                                              ctypes.c_double, P, P, P, ctypes.POINTER(ctypes.c_double)]),
+            "cg_simulate_stream": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_int32, P, P, P,
+                                                  ctypes.POINTER(ctypes.c_double)]),
             "cg_decode_layers": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                 ctypes.c_int32, ctypes.c_int32, P, P, S, P]),
             "cg_decode_paged": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
@@ -183,6 +187,48 @@ def cg_decode_paged(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: in
                                  int(nbytes), int(chunk_begin), int(chunk_end), _ptr(pools), _ptr(block_table),
                                  int(block_tokens), int(n_blocks), _ptr(ws), ws.numel() * ws.element_size(),
                                  _stream(stream))
+
+
+class cg_link_step(ctypes.Structure):
+    _fields_ = [("seconds", ctypes.c_double), ("bytes_per_s", ctypes.c_double)]
+
+
+def _link(trace):
+    arr = (cg_link_step * len(trace))(*[cg_link_step(float(a), float(b)) for a, b in trace])
+    return arr, len(trace)
+
+
+def cg_plan_levels(chunk_bytes, trace, initial_bytes_per_s: float, deadline_s: float, decode_s):
+    """Host-only level controller.  chunk_bytes: [n_chunks][n_levels] ints;
+    trace: [(seconds, bytes_per_s)]; decode_s: [n_chunks].
+    Returns (status, levels uint8[n], timeline float64[n,3], total seconds)."""
+    import numpy as np
+    cb = np.ascontiguousarray(chunk_bytes, dtype=np.uint64)
+    n, nl = cb.shape
+    ds = np.ascontiguousarray(decode_s, dtype=np.float64)
+    lv = np.zeros(n, np.uint8)
+    tl = np.zeros((n, 3), np.float64)
+    tot = ctypes.c_double(0.0)
+    arr, ns = _link(trace)
+    rc = lib().cg_plan_levels(n, nl, cb.ctypes.data, ctypes.cast(arr, ctypes.c_void_p), ns,
+                              float(initial_bytes_per_s), float(deadline_s), ds.ctypes.data, lv.ctypes.data,
+                              tl.ctypes.data, ctypes.byref(tot))
+    return rc, lv, tl, tot.value
+
+
+def cg_simulate_stream(chunk_bytes, trace, levels, decode_s):
+    """The same link/decode model for given levels -> (status, timeline, total)."""
+    import numpy as np
+    cb = np.ascontiguousarray(chunk_bytes, dtype=np.uint64)
+    n, nl = cb.shape
+    ds = np.ascontiguousarray(decode_s, dtype=np.float64)
+    lv = np.ascontiguousarray(levels, dtype=np.uint8)
+    tl = np.zeros((n, 3), np.float64)
+    tot = ctypes.c_double(0.0)
+    arr, ns = _link(trace)
+    rc = lib().cg_simulate_stream(n, nl, cb.ctypes.data, ctypes.cast(arr, ctypes.c_void_p), ns, lv.ctypes.data,
+                                  ds.ctypes.data, tl.ctypes.data, ctypes.byref(tot))
+    return rc, tl, tot.value
 
 
 def cg_read_status(ws) -> int:
