@@ -133,7 +133,10 @@ __device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *poo
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
 // access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
 // PAGED: token rows go to the paged cache po instead of kv.
-template <int T, bool PAGED>
+// BALLOT: word positions from one ballot per bit of the word counts instead
+// of a shuffle scan: more instructions, a shorter dependency chain, which
+// pays when few teams share the SM (small chunk ranges).
+template <int T, bool PAGED, bool BALLOT>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
@@ -229,6 +232,8 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 
   const int team = threadIdx.x / T, i = threadIdx.x % T, nteams = blockDim.x / T;
   const uint32_t tm = team_mask<T>();
+  [[maybe_unused]] uint32_t ltm = 0;  // lanes below this one
+  if constexpr (BALLOT) asm("mov.u32 %0, %%lanemask_lt;" : "=r"(ltm));
   const float4 st4 = *reinterpret_cast<const float4 *>(
       reinterpret_cast<const float *>(tables + lo.tb_step) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
   const float step[4] = {st4.x, st4.y, st4.z, st4.w};
@@ -400,16 +405,25 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           x[j] = ff[j] * (x[j] >> 16) + rr[j];
           needm |= (x[j] < kRansL) ? (1u << j) : 0u;
         }
-        const int cntw = __popc(needm) + 2 * __popc(escm);
+        const int cntw = __popc(needm) + 2 * __popc(escm);  // 0..12 words
         // ---- word positions: team-wide exclusive scan of the word counts
-        int incl = cntw;
+        uint32_t tot, excl;
+        if constexpr (BALLOT) {
+          const uint32_t b0 = __ballot_sync(tm, cntw & 1) & tm, b1 = __ballot_sync(tm, cntw & 2) & tm;
+          const uint32_t b2 = __ballot_sync(tm, cntw & 4) & tm, b3 = __ballot_sync(tm, cntw & 8) & tm;
+          tot = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2) + 8 * __popc(b3);
+          excl = __popc(b0 & ltm) + 2 * __popc(b1 & ltm) + 4 * __popc(b2 & ltm) + 8 * __popc(b3 & ltm);
+        } else {
+          int incl = cntw;
 #pragma unroll
-        for (int o = 1; o < T; o <<= 1) {
-          const int v = __shfl_up_sync(tm, incl, o, T);
-          if (i >= o) incl += v;
+          for (int o = 1; o < T; o <<= 1) {
+            const int v = __shfl_up_sync(tm, incl, o, T);
+            if (i >= o) incl += v;
+          }
+          tot = uint32_t(__shfl_sync(tm, incl, T - 1, T));
+          excl = uint32_t(incl - cntw);
         }
-        const uint32_t tot = uint32_t(__shfl_sync(tm, incl, T - 1, T));
-        uint32_t pos = p + uint32_t(incl - cntw);
+        uint32_t pos = p + excl;
         bool in_ring = true;
         if (p + tot > lim) {  // past the words known to be staged, or a refill may be due
         if (p + tot > nw) {
@@ -506,17 +520,31 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   }
 }
 
-template <int T, bool PAGED>
-cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
-                             uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po,
-                             int l0, int l1) {
-  if (teams > max_threads<T>() / T) teams = max_threads<T>() / T;
+template <int T, bool PAGED, bool BALLOT>
+cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
+                              uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po, int l0, int l1) {
   const size_t smem = size_t(kBuckets + kCdfRows) * lo.d * 2 + size_t(teams) * kRing * 2;
-  cudaError_t e = cudaFuncSetAttribute(k_decode<T, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e =
+      cudaFuncSetAttribute(k_decode<T, PAGED, BALLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
-  k_decode<T, PAGED><<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  k_decode<T, PAGED, BALLOT>
+      <<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
+}
+
+// chunks: the chunks in the range (an upper bound on a CTA's chunks).  A
+// CTA gets one team per chunk, but at least 512 threads so that the table
+// build is spread wide even when few chunks are decoded; teams without a
+// chunk only build.  Small ranges use the ballot word scan.
+template <int T, bool PAGED>
+cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
+                             uint16_t *kv, uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po,
+                             int l0, int l1) {
+  constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
+  const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
+  if (chunks < 12) return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+  return launch_decode_tpb<T, PAGED, false>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
 }
 
 template <int T>
