@@ -60,6 +60,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_max(values, world: int, device):
+    """Each value's maximum over the ranks (one all-reduce; as given at N=1):
+    the job's time is its slowest rank's."""
+    values = [float(v) for v in values]
+    if world == 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (max_ms * 1e-3) / 1e9
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -414,20 +432,12 @@ def main():
         del tb4, ws4
 
     # aggregate over ranks: max time, summed bytes
-    def agg_max(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    ms_dec, ms_enc, ms_fit = agg_max(ms["dec"]), agg_max(ms["enc"]), agg_max(ms["fit"])
-    ms_step_max = agg_max(ms_step)
-    ms_e2e = agg_max(statistics.mean(e2e_ms))
+    ms_dec, ms_enc, ms_fit, ms_step_max, ms_e2e = rank_max(
+        [ms["dec"], ms["enc"], ms["fit"], ms_step, statistics.mean(e2e_ms)], world, dev)
     fp16 = w.fp16_bytes
-    dec_gbs = world * fp16 / (ms_dec * 1e-3) / 1e9
-    enc_gbs = world * fp16 / (ms_enc * 1e-3) / 1e9
-    fit_gbs = world * fp16 / (ms_fit * 1e-3) / 1e9
+    dec_gbs = job_gbs(fp16, world, ms_dec)
+    enc_gbs = job_gbs(fp16, world, ms_enc)
+    fit_gbs = job_gbs(fp16, world, ms_fit)
     peak, peak_kind = peaks()
     dec_alg = nbytes + fp16
     enc_alg = fp16 + nbytes
@@ -466,7 +476,7 @@ def main():
         "roofline_encode": {"bound": "hbm", "achieved": enc_ach, "peak": peak, "unit": "GB/s",
                             "frac": enc_ach / peak, "traffic": traffic_for("k_encode", fp16), "kernel": "cg_encode",
                             "algorithmic_bytes_per_launch": enc_alg},
-        "e2e": {"value": world * fp16 / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": nbytes,
+        "e2e": {"value": job_gbs(fp16, world, ms_e2e), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
                 "d2h_bytes_per_step": fp16, "what": "pinned-host container -> cg_decode -> pinned-host KV"},
         "decode_paged": paged,
         "decode_layer_groups": lgroups,

@@ -59,7 +59,9 @@ __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wa
 constexpr uint32_t kRing = 512, kHalf = 256;
 // Symbol-search buckets: slot >> kBucketShift, kBuckets of them.
 constexpr uint32_t kBucketShift = 7, kBuckets = 1u << (16 - kBucketShift), kBucketSlots = 1u << kBucketShift;
-constexpr uint32_t kCdfRows = 258;  // cdf_0 .. cdf_257 (the last two stored as 0)
+constexpr uint32_t kCdfRows = 258;  // cdf_0 .. cdf_255, cdf_255 again, padding
+// Compact tables (two CTAs per SM): one u8 entry per 256-slot bucket.
+constexpr uint32_t kCBuckets = 256, kCBucketSlots = 256;
 
 // ---------------------------------------------------------------- index
 __global__ void k_decode_index(Layout lo, const uint8_t *__restrict__ tables,
@@ -133,16 +135,25 @@ __device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *poo
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
 // access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
 // PAGED: token rows go to the paged cache po instead of kv.
-// BALLOT: word positions from one ballot per bit of the word counts instead
-// of a shuffle scan: more instructions, a shorter dependency chain, which
-// pays when few teams share the SM (small chunk ranges).
-template <int T, bool PAGED, bool BALLOT>
+// COMPACT: for launches whose CTAs have few chunks (small chunk ranges,
+// mixed-level containers), tables small enough for two CTAs per SM: the
+// bucket table is lut8 [256 buckets][4 lanes x T] u8 holding only sa (the
+// densest pair's first symbol, at most 254) of each 256-slot bucket, in
+// lane order (thread i's four entries are word i: bank i); the search
+// loads cdf_sa, cdf_sa+1 and cdf_sa+2 and picks sa or sa + 1.  Such CTAs
+// also take word positions from one ballot per bit of the word counts
+// instead of a shuffle scan: more instructions, a shorter dependency chain,
+// which pays when few warps share the SM.
+template <int T, bool PAGED, bool COMPACT>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
+  constexpr bool BALLOT = COMPACT;
   extern __shared__ __align__(16) uint32_t smem[];
   uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [kBuckets][2][T][2]
-  uint16_t *cdfc = lut16 + kBuckets * kLpt * T;                      // [kCdfRows][2][T][2]
+  uint8_t *lut8 = reinterpret_cast<uint8_t *>(smem);               // COMPACT: [kCBuckets][T][4]
+  uint16_t *cdfc = COMPACT ? reinterpret_cast<uint16_t *>(lut8 + kCBuckets * kLpt * T)
+                           : lut16 + kBuckets * kLpt * T;              // [kCdfRows][2][T][2]
   uint16_t *rings = cdfc + kCdfRows * kLpt * T;                      // [teams][kRing] words
   __shared__ int s_bad;
 
@@ -186,6 +197,39 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   __syncthreads();
   // bucket entries: a thread walks 64 buckets of the two positions of one
   // 32-bit word, carrying the current symbol from bucket to bucket
+  if constexpr (COMPACT) {
+    // one lane's 64 buckets per thread: sa of each 256-slot bucket
+    for (int e = threadIdx.x; e < 4 * kRow; e += blockDim.x) {
+      const int c = e % kRow, b0 = 64 * (e / kRow);
+      const int ti = c >> 2, j = c & 3;
+      const uint16_t *colp = cdfc + (j >> 1) * 2 * T + 2 * ti + (j & 1);
+      uint32_t s = 0;
+#pragma unroll
+      for (uint32_t stp = 128; stp; stp >>= 1)
+        if (s + stp <= 255 && colp[(s + stp) * kRow] <= kCBucketSlots * b0) s += stp;
+      for (int bb = 0; bb < 64; bb++) {
+        const uint32_t slot0 = kCBucketSlots * (b0 + bb);
+        while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
+        uint32_t sa = s;
+        {
+          uint32_t t = s, beg = slot0, prev = 0, best = 0;
+          for (;;) {
+            const uint32_t nt = t < 255 ? uint32_t(colp[(t + 1) * kRow]) : kM;
+            const uint32_t cnt = min(nt, slot0 + kCBucketSlots) - beg;
+            if (t > s && prev + cnt > best) {
+              best = prev + cnt;
+              sa = t - 1;
+            }
+            if (t == 255 || nt >= slot0 + kCBucketSlots) break;
+            prev = cnt;
+            beg = nt;
+            t++;
+          }
+        }
+        lut8[(b0 + bb) * kRow + c] = uint8_t(min(sa, 254u));
+      }
+    }
+  } else
   for (int e = threadIdx.x; e < 8 * 2 * T; e += blockDim.x) {
     const int wd = e % (2 * T), b0 = 64 * (e / (2 * T));
 #pragma unroll
@@ -240,6 +284,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   // thread i's entries: u16 index row * (4T) + (j>>1)*2T + 2i + (j&1); with
   // T = 32 a row is 256 bytes, so the bucket row of state x is x & 0xFF00.
   const uint16_t *lt = lut16 + 2 * i;
+  [[maybe_unused]] const uint8_t *lt8 = lut8 + kLpt * i;  // COMPACT: lane j of thread i at lt8[b * 4T + j]
   const uint16_t *ct = cdfc + 2 * i;
 
   for (int idx = team; idx < cnt; idx += nteams) {
@@ -352,15 +397,28 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           const int cj = (j >> 1) * T * 2 + (j & 1);
-          const uint32_t b = (x[j] >> kBucketShift) & (kBuckets - 1);
-          const uint32_t lu = lt[b * (kLpt * T) + cj];
-          // carry out of the low byte adds one when the slot is past s0's part of the bucket
-          const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
-          const uint32_t c0 = ct[sj * (kLpt * T) + cj];
-          const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
-          ff[j] = c1 - c0;
-          rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
-          sy[j] = sj;
+          if constexpr (COMPACT) {
+            const uint32_t slot = x[j] & 0xFFFFu;
+            const uint32_t sa = lt8[(slot >> 8) * (kLpt * T) + j];
+            const uint32_t c0 = ct[sa * (kLpt * T) + cj];
+            const uint32_t c1 = ct[(sa + 1) * (kLpt * T) + cj];
+            const uint32_t c2 = ct[(sa + 2) * (kLpt * T) + cj];
+            const bool up = slot >= c1;
+            const uint32_t clo = up ? c1 : c0;
+            ff[j] = (up ? c2 : c1) - clo;
+            rr[j] = slot - clo;  // wraps above 0xFFFF when the slot is below sa
+            sy[j] = sa + (up ? 1u : 0u);
+          } else {
+            const uint32_t b = (x[j] >> kBucketShift) & (kBuckets - 1);
+            const uint32_t lu = lt[b * (kLpt * T) + cj];
+            // carry out of the low byte adds one when the slot is past s0's part of the bucket
+            const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
+            const uint32_t c0 = ct[sj * (kLpt * T) + cj];
+            const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
+            ff[j] = c1 - c0;
+            rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
+            sy[j] = sj;
+          }
           sl[j] = rr[j] >= ff[j];
         }
         // Slow lanes (well under 1%): a binary search in the lane's own table
@@ -374,14 +432,26 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             if (sl[j]) {
               const int cj = (j >> 1) * T * 2 + (j & 1);
               const uint32_t slot = x[j] & 0xFFFFu;
-              const uint32_t b = slot >> kBucketShift;
               uint32_t lo = sy[j], hi = lo;
-              if (rr[j] > 0xFFFFu) {  // below the pair: down to the previous bucket's pair
-                hi = lo - 1;
-                lo = b > 0 ? (lt[(b - 1) * (kLpt * T) + cj] >> 8) : 0u;
-              } else if (lo < 255) {  // above the pair (255: the escape symbol, already found)
-                lo += 1;  // cdf_lo <= slot is known
-                hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
+              if constexpr (COMPACT) {
+                // the neighbours' sa bound the symbol (sa + 1 above: sa stops at 254)
+                const uint32_t b = slot >> 8;
+                if (rr[j] > 0xFFFFu) {
+                  hi = lo - 1;
+                  lo = b > 0 ? uint32_t(lt8[(b - 1) * (kLpt * T) + j]) : 0u;
+                } else if (lo < 255) {
+                  lo += 1;
+                  hi = b + 1 < kCBuckets ? uint32_t(lt8[(b + 1) * (kLpt * T) + j]) + 1u : 255u;
+                }
+              } else {
+                const uint32_t b = slot >> kBucketShift;
+                if (rr[j] > 0xFFFFu) {  // below the pair: down to the previous bucket's pair
+                  hi = lo - 1;
+                  lo = b > 0 ? (lt[(b - 1) * (kLpt * T) + cj] >> 8) : 0u;
+                } else if (lo < 255) {  // above the pair (255: the escape symbol, already found)
+                  lo += 1;  // cdf_lo <= slot is known
+                  hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
+                }
               }
               {
                 while (lo < hi) {
@@ -520,30 +590,43 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   }
 }
 
-template <int T, bool PAGED, bool BALLOT>
+template <int T, bool PAGED, bool COMPACT>
 cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
                               uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po, int l0, int l1) {
-  const size_t smem = size_t(kBuckets + kCdfRows) * lo.d * 2 + size_t(teams) * kRing * 2;
+  const size_t tabs = COMPACT ? size_t(kCBuckets) * lo.d + size_t(kCdfRows) * lo.d * 2
+                              : size_t(kBuckets + kCdfRows) * lo.d * 2;
+  const size_t smem = tabs + size_t(teams) * kRing * 2;
   cudaError_t e =
-      cudaFuncSetAttribute(k_decode<T, PAGED, BALLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      cudaFuncSetAttribute(k_decode<T, PAGED, COMPACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two compact CTAs fit
+    e = cudaFuncSetAttribute(k_decode<T, PAGED, COMPACT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
-  k_decode<T, PAGED, BALLOT>
+  k_decode<T, PAGED, COMPACT>
       <<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
 }
 
-// chunks: the chunks in the range (an upper bound on a CTA's chunks).  A
-// CTA gets one team per chunk, but at least 512 threads so that the table
-// build is spread wide even when few chunks are decoded; teams without a
-// chunk only build.  Small ranges use the ballot word scan.
+// chunks: the chunks in the range.  A CTA decodes one (level, head), one
+// team per chunk of that level.  When a CTA can be expected to hold at
+// most 12 chunks (a range of at most 12, or several levels sharing the
+// range thinly: twice the mean per level at most 12), the compact tables
+// let two CTAs share an SM, with 8 to 12 teams each (a team takes a second
+// chunk if its level has more).  Otherwise a CTA has one team per chunk,
+// and at least 512 threads so that the table build is spread wide; teams
+// without a chunk only build.
 template <int T, bool PAGED>
 cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                              uint16_t *kv, uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po,
                              int l0, int l1) {
   constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
+  const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
+  if (T == 32 && (chunks <= 12 || 2 * per_level <= 12)) {
+    const int teams = chunks <= 12 ? (chunks < 8 ? 8 : chunks) : 12;
+    return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+  }
   const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
-  if (chunks < 12) return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
   return launch_decode_tpb<T, PAGED, false>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
 }
 

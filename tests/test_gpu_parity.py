@@ -42,6 +42,13 @@ CASES = {
                                  (0.1,), None, None),
     "many_chunks_teams": (synth.GenSpec(L=1, H=1, d=128, S=2100, seed=29, innov="t3", rho=(0.85, 0.99)),
                           50, 10, 127, (0.1, 0.3), None, [i % 2 for i in range(42)]),
+    # d = 128 with few chunks per (level, head): the compact-table decoder;
+    # here one level holds 21 of 24 chunks, more than a CTA's 12 teams
+    "d128_compact_second_round": (synth.GenSpec(L=1, H=2, d=128, S=960, seed=30, innov="t3", rho=(0.85, 0.99),
+                                                n_outliers=2, outlier_scale=20.0), 40, 10, 127,
+                                  (0.05, 0.1, 0.2, 0.4), None, [0] * 21 + [1, 2, 3]),
+    "d128_compact_escapes_R3": (synth.GenSpec(L=1, H=1, d=128, S=300, seed=31, innov="t3", rho=(0.85, 0.9)),
+                                100, 10, 3, (0.05,), None, None),
 }
 
 
