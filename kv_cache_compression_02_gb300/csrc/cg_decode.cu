@@ -469,13 +469,13 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             }
           }
         }
-        uint32_t needm = 0;
+        bool nd4[4];
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           x[j] = ff[j] * (x[j] >> 16) + rr[j];
-          needm |= (x[j] < kRansL) ? (1u << j) : 0u;
+          nd4[j] = x[j] < kRansL;
         }
-        const int cntw = __popc(needm) + 2 * __popc(escm);  // 0..12 words
+        const int cntw = int(nd4[0]) + int(nd4[1]) + int(nd4[2]) + int(nd4[3]) + 2 * __popc(escm);  // 0..12 words
         // ---- word positions: team-wide exclusive scan of the word counts
         uint32_t tot, excl;
         if constexpr (BALLOT) {
@@ -529,7 +529,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           for (int j = 0; j < 4; j++) {
             {
               const uint32_t w = ring[pos & (kRing - 1)];  // read unconditionally, use if needed
-              const bool nd = (needm >> j) & 1u;
+              const bool nd = nd4[j];
               x[j] = nd ? __byte_perm(w, x[j], 0x5410) : x[j];  // x<<16 | w
               pos += nd ? 1u : 0u;
             }
@@ -540,7 +540,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         } else {  // escapes: the raw q follows the lane's renormalisation word
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(ring[pos++ & (kRing - 1)]), x[j], 0x5410);
+            if (nd4[j]) x[j] = __byte_perm(uint32_t(ring[pos++ & (kRing - 1)]), x[j], 0x5410);
             if ((escm >> j) & 1u) {
               const int q = int(uint32_t(ring[pos & (kRing - 1)]) | (uint32_t(ring[(pos + 1) & (kRing - 1)]) << 16));
               pos += 2;
@@ -556,7 +556,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         if (escm == 0) {
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);  // x<<16 | w
+            if (nd4[j]) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);  // x<<16 | w
             // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
             const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
             v[j] = __fmaf_rn(qf, step[j], ah[j]);
@@ -564,7 +564,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         } else {  // escapes: the raw q follows the lane's renormalisation word
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            if ((needm >> j) & 1u) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
+            if (nd4[j]) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
             if ((escm >> j) & 1u) {
               const int q = int(uint32_t(words[pos]) | (uint32_t(words[pos + 1]) << 16));
               pos += 2;
