@@ -165,7 +165,7 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
         for (int j = 3; j >= 0; j--) {
           const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
           const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
-          esc[j] = !(q >= -R && q <= R);
+          esc[j] = uint32_t(q) + uint32_t(R) > uint32_t(2 * R);  // |q| > R, in unsigned arithmetic
           const int sym = esc[j] ? kEsc : q + 127;
           const uint32_t e = etab[(sym * kLpt + j) * T + i];
           const uint32_t f = e >> 16, c = e & 0xFFFFu;
