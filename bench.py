@@ -429,12 +429,14 @@ def main():
         cg.check(cg.cg_fit_tables(cfg4, kv, tb4, ws4, stream), "cg_fit_tables (4 levels)")
         nk = w.n_chunks
         sizes = np.zeros((nk, len(lb4)), np.int64)
+        singles = []  # the context encoded once per level
         for lv in range(len(lb4)):
             cg.check(cg.cg_encode(cfg4, tb4, kv, np.full(nk, lv, np.uint8), out, nbytes_d, ws4, stream),
                      "cg_encode (one level)")
             torch.cuda.synchronize()
             cg.check(cg.cg_read_status(ws4), "encode (one level)")
             n_lv = int(nbytes_d.item())
+            singles.append(out[:n_lv].clone())
             offs = np.append(out[64:64 + 8 * nk].cpu().numpy().view(np.uint64).astype(np.int64), n_lv)
             sizes[:, lv] = np.diff(offs)
             sizes[0, lv] += offs[0]  # the header and chunk index go out with chunk 0
@@ -445,9 +447,23 @@ def main():
         rc, lv_plan, _, total = cg.cg_plan_levels(sizes, trace, nominal, deadline, dec)
         cg.check(rc, "cg_plan_levels")
         fixed = {f"level_{lv}": cg.cg_simulate_stream(sizes, trace, [lv] * nk, dec)[2] for lv in range(len(lb4))}
+        # the planned container from the per-level ones (device copies), checked
+        # against a direct encode with the planned levels
+        ws_a = cg.empty_u8(cg.cg_workspace_bytes(cfg4, cg.CG_OP_ASSEMBLE))
+        asm = cg.empty_u8(cg.cg_encode_bound(cfg4))
+        nb_a = torch.zeros(1, dtype=torch.int64, device=dev)
+        ta, tb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ta.record(stream)
+        cg.check(cg.cg_assemble(cfg4, singles, lv_plan, asm, nb_a, ws_a, stream), "cg_assemble")
+        tb_.record(stream)
         cg.check(cg.cg_encode(cfg4, tb4, kv, lv_plan, out, nbytes_d, ws4, stream), "cg_encode (planned)")
         torch.cuda.synchronize()
+        cg.check(cg.cg_read_status(ws_a), "assemble (planned)")
         n_plan = int(nbytes_d.item())
+        if int(nb_a.item()) != n_plan or not torch.equal(asm[:n_plan], out[:n_plan]):
+            raise RuntimeError("assembled container differs from the direct encode")
+        assemble_ms = ta.elapsed_time(tb_)
+        del asm, singles
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         cg.check(cg.cg_decode(cfg4, tb4, out, n_plan, 0, -1, kv_out, ws4, stream), "cg_decode (planned)")
@@ -457,7 +473,7 @@ def main():
         adaptive = {"level_base": list(lb4), "link": "400 Gb/s, 100 Gb/s from 20 to 45 ms, then 400 Gb/s",
                     "deadline_s": deadline, "levels": lv_plan.tolist(), "total_s": total,
                     "met_deadline": bool(total <= deadline), "fixed_level_total_s": fixed,
-                    "container_bytes": n_plan, "decode_ms": a.elapsed_time(b)}
+                    "container_bytes": n_plan, "assemble_ms": assemble_ms, "decode_ms": a.elapsed_time(b)}
         del tb4, ws4
 
     # aggregate over ranks: max time, summed bytes

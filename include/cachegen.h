@@ -91,7 +91,7 @@ typedef struct {
     int32_t alphabet_radius;  /* R: |q| <= R coded directly, else escape   */
 } cg_params;
 
-enum { CG_OP_FIT = 0, CG_OP_ENCODE = 1, CG_OP_DECODE = 2 };
+enum { CG_OP_FIT = 0, CG_OP_ENCODE = 1, CG_OP_DECODE = 2, CG_OP_ASSEMBLE = 3 };
 
 /* Size in bytes of the tables blob for (dims, params).  0 on bad input. */
 size_t cg_tables_bytes(const cg_dims *dims, const cg_params *params);
@@ -138,6 +138,29 @@ cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *ta
                     const void *kv_dev, const uint8_t *chunk_level_host, void *out_dev,
                     uint64_t out_capacity, uint64_t *out_bytes_dev, void *ws_dev,
                     size_t ws_bytes, void *stream);
+
+/* The container cg_encode would make for levels chunk_level_host, built
+ * from containers of the same KV encoded at one level each (with the same
+ * tables): chunk k is copied verbatim from level_containers[chunk_level_host[k]],
+ * behind a new header and chunk index.  A serving system can encode a
+ * context once per level and assemble any level choice (e.g. from
+ * cg_plan_levels) with device copies only (gptget summary of arXiv
+ * 2310.07240, Methodology: compression adjusted to the bandwidth while
+ * chunks stream).
+ *   level_containers: host array of n_levels device pointers (16-byte
+ *                     aligned; may be NULL for levels no chunk uses);
+ *   level_bytes:      host array of their sizes;
+ *   out_dev, out_capacity, out_bytes_dev: as for cg_encode (the size is
+ *                     written even when it exceeds out_capacity);
+ *   ws_dev:           cg_workspace_bytes(CG_OP_ASSEMBLE) bytes.
+ * Device errors: CG_ERR_CORRUPT (a source header, index entry or chunk
+ * header that does not match dims/params and the requested level),
+ * CG_ERR_CAPACITY (nothing written).  The result is bit-identical to
+ * cg_encode's for the same levels. */
+cg_status cg_assemble(const cg_dims *dims, const cg_params *params, const void *const *level_containers,
+                      const uint64_t *level_bytes, const uint8_t *chunk_level_host, void *out_dev,
+                      uint64_t out_capacity, uint64_t *out_bytes_dev, void *ws_dev, size_t ws_bytes,
+                      void *stream);
 
 /* Decode chunks [chunk_begin, chunk_end) of a container into the full KV
  * buffer kv_dev (fp16 [L][2][H][S][d]; only those chunks' tokens are

@@ -16,7 +16,7 @@ import numpy as np
 from . import build as _build
 
 CG_OK, CG_ERR_INVALID_ARG, CG_ERR_NONFINITE, CG_ERR_CAPACITY, CG_ERR_CORRUPT, CG_ERR_CUDA, CG_ERR_TIMEOUT = range(7)
-CG_OP_FIT, CG_OP_ENCODE, CG_OP_DECODE = 0, 1, 2
+CG_OP_FIT, CG_OP_ENCODE, CG_OP_DECODE, CG_OP_ASSEMBLE = 0, 1, 2, 3
 
 
 class cg_dims(ctypes.Structure):
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "cg_read_status": (ctypes.c_int, [P]),
             "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                  P, P, ctypes.POINTER(ctypes.c_void_p)]),
+            "cg_assemble": (ctypes.c_int, [D, Pr, P, P, P, P, ctypes.c_uint64, P, P, S, P]),
             "cg_plan_levels": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_int32, ctypes.c_double,
                                               ctypes.c_double, P, P, P, ctypes.POINTER(ctypes.c_double)]),
             "cg_simulate_stream": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_int32, P, P, P,
@@ -150,6 +151,21 @@ def cg_encode(cfg: Config, tables, kv, chunk_levels, out, out_bytes, ws, stream=
     return lib().cg_encode(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(tables), _ptr(kv),
                            lv.ctypes.data, _ptr(out), out.numel() * out.element_size(), _ptr(out_bytes),
                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def cg_assemble(cfg: Config, level_containers, chunk_levels, out, out_bytes, ws, stream=None) -> int:
+    """level_containers: one device uint8 tensor per level (None where no
+    chunk uses the level), each holding exactly its container's bytes."""
+    nl = cfg.params.n_levels
+    ptrs = (ctypes.c_void_p * nl)(*[None if c is None else _ptr(c) for c in level_containers])
+    sizes = (ctypes.c_uint64 * nl)(*[0 if c is None else c.numel() for c in level_containers])
+    lv = np.ascontiguousarray(np.asarray(chunk_levels, dtype=np.uint8))
+    if lv.size != cfg.n_chunks or len(level_containers) != nl:
+        return CG_ERR_INVALID_ARG
+    return lib().cg_assemble(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), ctypes.cast(ptrs, ctypes.c_void_p),
+                             ctypes.cast(sizes, ctypes.c_void_p), lv.ctypes.data, _ptr(out),
+                             out.numel() * out.element_size(), _ptr(out_bytes), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
 
 
 def cg_decode(cfg: Config, tables, bitstream, nbytes: int, chunk_begin: int, chunk_end: int, kv, ws,

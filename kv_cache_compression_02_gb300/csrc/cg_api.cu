@@ -88,6 +88,7 @@ size_t cg_workspace_bytes(const cg_dims *dims, const cg_params *params, int op) 
     case CG_OP_FIT: return size_t(fit_ws(lo).bytes);
     case CG_OP_ENCODE: return size_t(enc_ws(lo).bytes);
     case CG_OP_DECODE: return size_t(dec_ws(lo).bytes);
+    case CG_OP_ASSEMBLE: return size_t(assemble_workspace_bytes(lo));
   }
   return 0;
 }

@@ -26,6 +26,9 @@ cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *table
 cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, uint8_t *out,
                                 uint64_t cap, uint64_t *out_bytes, cudaStream_t st);
 
+// cg_assemble.cu
+uint64_t assemble_workspace_bytes(const Layout &lo);
+
 // cg_decode.cu
 // A paged KV cache: the pool of layer l, K/V kv is fp16
 // [n_blocks][H][bt][d] at pools[2 l + kv]; token t of the sequence is row

@@ -91,3 +91,14 @@ def test_invalid_arguments(lib):
     assert lib.cg_decode_paged(*args(fake, None, 4, 4)) == cg.CG_ERR_INVALID_ARG
     assert lib.cg_decode_paged(*args(fake, fake, 0, 4)) == cg.CG_ERR_INVALID_ARG
     assert lib.cg_decode_paged(*args(fake, fake, 4, 0)) == cg.CG_ERR_INVALID_ARG
+    # cg_assemble: missing arrays or a level out of range, rejected before any CUDA call
+    lv = (ctypes.c_uint8 * 1)(0)
+    ptrs = (ctypes.c_void_p * 1)(fake)
+    sizes = (ctypes.c_uint64 * 1)(1 << 20)
+    asm = lambda p, z, l: (ctypes.byref(ok.dims), ctypes.byref(ok.params), p, z, l, fake, 1 << 20, fake,  # noqa: E731
+                           fake, 1 << 20, None)
+    assert lib.cg_assemble(*asm(None, sizes, lv)) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_assemble(*asm(ptrs, None, lv)) == cg.CG_ERR_INVALID_ARG
+    assert lib.cg_assemble(*asm(ptrs, sizes, None)) == cg.CG_ERR_INVALID_ARG
+    bad = (ctypes.c_uint8 * 1)(1)  # level 1 of a one-level configuration
+    assert lib.cg_assemble(*asm(ptrs, sizes, bad)) == cg.CG_ERR_INVALID_ARG
