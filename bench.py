@@ -185,6 +185,47 @@ def cpu_oracle_decode_rate(w, host_np, budget_s=10.0):
     return nbytes / spent, spent, streams
 
 
+def _oracle_worker(args):
+    """One process of the all-core oracle run: heads si = first, first +
+    stride, ... of workload `name`, generated here; the oracle fits and
+    encodes each (untimed) and decodes its chunk streams until budget_s of
+    decode time is spent.  Returns (fp16 bytes decoded, decode seconds)."""
+    name, first, stride, budget_s = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from kv_cache_compression_02_gb300 import synth, workloads as W
+    w = W.BY_NAME[name]
+    cd = oracle.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
+    out = np.zeros((w.S, w.d), np.uint16)
+    spent, nbytes = 0.0, 0
+    for si in range(first, w.L * 2 * w.H, stride):
+        l, kv, h = si // (2 * w.H), (si // w.H) % 2, si % w.H
+        head = synth.head(w.gen, l, kv, h)
+        m = [0.5, 1.0, 2.0][(3 * l) // w.L]
+        rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
+        for k in range(cd.n_chunks):
+            n, blk, sc, anc = oracle.encode_stream(cd, head, k, st, rp, cdf)
+            t0 = time.perf_counter()
+            assert oracle.decode_stream(cd, blk, k, st, cdf, sc, anc, out) == 0
+            spent += time.perf_counter() - t0
+            nbytes += min(w.C, w.S - k * w.C) * w.d * 2
+            if spent >= budget_s:
+                return nbytes, spent
+    return nbytes, spent
+
+
+def cpu_oracle_decode_rate_all_cores(name, budget_s=10.0):
+    """The oracle decode on every host core at once (one spawned process per
+    core, each on its own heads): summed fp16 bytes/s, and the core count."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [(name, i * 7, n * 7, budget_s) for i in range(n)])
+    return sum(b / t for b, t in res if t > 0), n
+
+
 def run_reference(args):
     """The CPU oracle on the machine's host cores (reference arm)."""
     rank, world, _ = dist_env()
@@ -499,11 +540,13 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        rate, spent, nstreams = cpu_oracle_decode_rate(w, host.numpy().view(np.uint16))
-        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"oracle decode of {nstreams} streams ({w.C} tokens x {w.d} lanes each, heads spread "
-                         f"over the layers), "
-                         f"{spent:.1f} s"}
+        rate, spent, nstreams = cpu_oracle_decode_rate(w, host.numpy().view(np.uint16), budget_s=8.0)
+        rate_all, cores = cpu_oracle_decode_rate_all_cores(w.name, budget_s=8.0)
+        cpu = {"value": rate_all / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"oracle decode of chunk streams ({w.C} tokens x {w.d} lanes) of heads spread over the "
+                         f"layers, one process per core, 8 s of decode each",
+               "single_core": {"value": rate / 1e9, "unit": "GB/s", "cores": 1,
+                               "sample": f"{nstreams} streams, {spent:.1f} s"}}
     line = {
         "metric": METRIC, "value": dec_gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",

@@ -47,6 +47,10 @@ CASES = {
     "d128_compact_second_round": (synth.GenSpec(L=1, H=2, d=128, S=960, seed=30, innov="t3", rho=(0.85, 0.99),
                                                 n_outliers=2, outlier_scale=20.0), 40, 10, 127,
                                   (0.05, 0.1, 0.2, 0.4), None, [0] * 21 + [1, 2, 3]),
+    # separate K and V multipliers per layer (finer steps for keys)
+    "d32_kv_asymmetric": (synth.GenSpec(L=3, H=2, d=32, S=400, seed=32, innov="t3", rho=(0.85, 0.99), n_outliers=1,
+                                        outlier_scale=20.0), 128, 10, 127, (0.1,),
+                          np.array([[0.25, 1.0], [0.5, 2.0], [1.0, 4.0]], np.float32), None),
     "d128_compact_escapes_R3": (synth.GenSpec(L=1, H=1, d=128, S=300, seed=31, innov="t3", rho=(0.85, 0.9)),
                                 100, 10, 3, (0.05,), None, None),
 }

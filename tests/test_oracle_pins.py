@@ -486,3 +486,59 @@ def test_paged_layout_hand_example(orc):
     part = orc.paged_from_contiguous(kv, [2, 0, 1], 2, 3, fill=0, tokens=[2, 3])
     assert (part[0, :, 2] == 0).all() and (part[0, :, 1] == 0).all()
     assert part[0, 0, 0, 0, 0, 0] == 21 and part[0, 0, 0, 0, 1, 0] == 31
+
+
+def test_kv_asymmetric_multipliers(orc):
+    """Separate K and V multipliers per layer (Guide to CacheGen, pillar 1:
+    keys need finer steps than values): with the same data in K and V, a
+    channel's V step over its K step is the multiplier ratio, exactly for a
+    power-of-two ratio; every table is otherwise what one multiplier gives."""
+    spec = synth.GenSpec(L=2, H=1, d=8, S=200, seed=71, innov="laplace", rho=(0.9, 0.9), n_outliers=0)
+    x = synth.generate(spec)
+    x[:, 1] = x[:, 0]  # V = K
+    cd = orc.Codec(2, 1, 8, 200, C=100, G=10)
+    lm = np.array([[0.25, 1.0], [0.5, 2.0]], np.float32)  # V steps 4x the K steps
+    rc, tb = orc.fit_tables(cd, [0.1], lm, x)
+    assert rc == 0
+    step_, recip, cdf = orc.tables_views(tb, cd, 1)
+    for l in range(2):
+        big = step_[0, l, 0] > 2.0 ** -12 * 4  # away from the step floor
+        assert np.array_equal(step_[0, l, 1][big], 4 * step_[0, l, 0][big])
+    # K of layer 0 equals a fit with that multiplier for both K and V
+    rc, tb_k = orc.fit_tables(cd, [0.1], np.array([[0.25, 0.25], [0.5, 0.5]], np.float32), x)
+    s_k, _, c_k = orc.tables_views(tb_k, cd, 1)
+    assert np.array_equal(s_k[0, :, 0], step_[0, :, 0]) and np.array_equal(c_k[0, :, 0], cdf[0, :, 0])
+    cont_rc, cont, _ = orc.encode(cd, 1, tb, x, np.zeros(cd.n_chunks, np.uint8))
+    rc, y = orc.decode(tb, cont)
+    assert cont_rc == 0 and rc == 0
+    err = np.abs(y.view(np.float16).astype(np.float64) - x.view(np.float16).astype(np.float64))
+    assert err[:, 0].max() < err[:, 1].max()  # finer K steps, smaller K error
+
+
+def test_outlier_channel_does_not_touch_other_channels(orc):
+    """Outlier channels are kept from corrupting the regular channels'
+    distributions (Guide to CacheGen, pillar 3: the sparse outlier table).
+    Here every channel has its own step and frequency table, so scaling one
+    channel by 20x leaves every other channel's table and decoded values
+    unchanged."""
+    spec = synth.GenSpec(L=1, H=2, d=16, S=300, seed=72, innov="t3", rho=(0.9, 0.9), n_outliers=0)
+    x = synth.generate(spec)
+    y = x.copy()
+    ch = y[0, 0, 1, :, 5].view(np.float16).astype(np.float32) * 20
+    y[0, 0, 1, :, 5] = ch.astype(np.float16).view(np.uint16)
+    cd = orc.Codec(1, 2, 16, 300, C=100, G=10)
+    rc, tx = orc.fit_tables(cd, [0.1], None, x)
+    rc2, ty = orc.fit_tables(cd, [0.1], None, y)
+    assert rc == rc2 == 0
+    sx, _, cx = orc.tables_views(tx, cd, 1)
+    sy, _, cy = orc.tables_views(ty, cd, 1)
+    other = np.ones(2 * 16, bool)
+    other[16 + 5] = False  # head 1, channel 5 of K
+    assert np.array_equal(sx[0, 0, 0][other], sy[0, 0, 0][other])
+    assert np.array_equal(cx[0, 0, 0][other], cy[0, 0, 0][other])
+    assert not np.array_equal(sx[0, 0, 0][~other], sy[0, 0, 0][~other])
+    dx = orc.decode(tx, orc.encode(cd, 1, tx, x, np.zeros(3, np.uint8))[1])[1]
+    dy = orc.decode(ty, orc.encode(cd, 1, ty, y, np.zeros(3, np.uint8))[1])[1]
+    mask = np.ones(dx.shape, bool)
+    mask[0, 0, 1, :, 5] = False
+    assert np.array_equal(dx[mask], dy[mask])
