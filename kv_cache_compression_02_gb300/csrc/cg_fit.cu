@@ -15,6 +15,8 @@
 // All three are HBM-streaming kernels (no contraction, no tensor cores).
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "cg_kernels.cuh"
 
 namespace cg {
@@ -76,15 +78,66 @@ __device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint32_t (&q
       : "r"(v0), "r"(v1), "r"(v2));
 }
 
+// The head's rows stream through shared memory in 16 KB tiles, four in
+// flight: one thread issues each tile as a bulk asynchronous copy that
+// completes on the tile's mbarrier, so the loads need no registers and the
+// next tiles land while this one is summed.
+constexpr uint32_t kStatsTile = 16384, kStatsStages = 4;
+constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+  for (uint32_t it = 0; it < kWaitLimit; it++) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 __global__ void __launch_bounds__(kStatsThreads, 2)
 k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables,
         const float *__restrict__ mult, Bases bases, uint32_t *status) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];  // kStatsStages tiles, then the reduction
+  __shared__ __align__(8) uint64_t bars[kStatsStages];
+  __shared__ int s_timeout;
   const int si = blockIdx.x;
   const int tpr = lo.d / 4;                 // threads per token row
-  const int rows = kStatsThreads / tpr;     // token rows in flight
+  const int rows = kStatsThreads / tpr;     // token rows summed side by side
   const int col = threadIdx.x % tpr, row = threadIdx.x / tpr;
-  const uint16_t *head = kv + uint64_t(si) * lo.S * lo.d + 4 * col;
+  const uint32_t row_bytes = 2u * uint32_t(lo.d);
+  const uint8_t *head = reinterpret_cast<const uint8_t *>(kv + uint64_t(si) * lo.S * lo.d);
+  const uint64_t head_bytes = uint64_t(lo.S) * row_bytes;  // a multiple of 16
+  const uint64_t ntiles = (head_bytes + kStatsTile - 1) / kStatsTile;
+
+  auto issue = [&](uint64_t t) {  // tile t into stage t % kStatsStages
+    const uint32_t st = uint32_t(t % kStatsStages);
+    const uint64_t left = head_bytes - t * kStatsTile;
+    const uint32_t bytes = uint32_t(left < kStatsTile ? left : kStatsTile);
+    const uint32_t bar = smem_addr(&bars[st]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem + st * kStatsTile)),
+        "l"(head + t * kStatsTile), "r"(bytes), "r"(bar)
+        : "memory");
+  };
+  if (threadIdx.x == 0) {
+    s_timeout = 0;
+    for (uint32_t st = 0; st < kStatsStages; st++)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[st])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (uint64_t t = 0; t < ntiles && t < kStatsStages; t++) issue(t);
+  }
+  __syncthreads();
 
   int64_t T[4];
   uint32_t Q[4][4];
@@ -94,20 +147,32 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     Q[i][0] = Q[i][1] = Q[i][2] = Q[i][3] = 0;
   }
   uint32_t bad = 0;  // bit 15 of a half: an all-ones exponent (Inf or NaN) was seen
-  for (int64_t t0 = row; t0 < lo.S; t0 += 4 * int64_t(rows)) {
-    uint2 vv[4];
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int64_t t = t0 + int64_t(u) * rows;
-      vv[u] = t < lo.S ? __ldg(reinterpret_cast<const uint2 *>(head + t * lo.d)) : make_uint2(0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const uint32_t hw[4] = {vv[u].x & 0xFFFFu, vv[u].x >> 16, vv[u].y & 0xFFFFu, vv[u].y >> 16};
-      bad |= ((vv[u].x & 0x7C007C00u) + 0x04000400u) | ((vv[u].y & 0x7C007C00u) + 0x04000400u);
+  uint64_t t = 0;
+  for (; t < ntiles; t++) {
+    const uint32_t st = uint32_t(t % kStatsStages);
+    if (!mbar_wait(smem_addr(&bars[st]), uint32_t(t / kStatsStages) & 1u)) s_timeout = 1;
+    __syncthreads();  // every thread knows whether the tile landed
+    if (s_timeout) break;
+    const uint8_t *tile = smem + st * kStatsTile;
+    const uint64_t left = head_bytes - t * kStatsTile;
+    const uint32_t nr = uint32_t(left < kStatsTile ? left : kStatsTile) / row_bytes;
+    for (uint32_t r = row; r < nr; r += rows) {
+      const uint2 vv = *reinterpret_cast<const uint2 *>(tile + r * row_bytes + 8 * col);
+      const uint32_t hw[4] = {vv.x & 0xFFFFu, vv.x >> 16, vv.y & 0xFFFFu, vv.y >> 16};
+      bad |= ((vv.x & 0x7C007C00u) + 0x04000400u) | ((vv.y & 0x7C007C00u) + 0x04000400u);
 #pragma unroll
       for (int i = 0; i < 4; i++) acc_moments(hw[i], T[i], Q[i]);  // a non-finite value only spoils a flagged result
     }
+    __syncthreads();  // the stage has been read: it can take the next tile
+    if (threadIdx.x == 0 && t + kStatsStages < ntiles) issue(t + kStatsStages);
+  }
+  if (s_timeout) {  // a copy never completed: wait (bounded) for the ones in flight, then give up
+    if (threadIdx.x == 0) {
+      atomicOr(status, kStTimeout);
+      for (uint64_t u = t; u < ntiles && u < t + kStatsStages; u++)
+        mbar_wait(smem_addr(&bars[u % kStatsStages]), uint32_t(u / kStatsStages) & 1u);
+    }
+    return;
   }
   if (bad & 0x80008000u) atomicOr(status, kStNonfinite);
 
@@ -359,7 +424,7 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
 cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
                          Bases bases, uint32_t *status, cudaStream_t st) {
   const int rows = kStatsThreads / (lo.d / 4);
-  const size_t smem = size_t(rows) * lo.d * 24;
+  const size_t smem = std::max(size_t(kStatsStages) * kStatsTile, size_t(rows) * lo.d * 24);
   cudaError_t e = cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   k_stats<<<lo.nstr, kStatsThreads, smem, st>>>(lo, kv, tables, mult, bases, status);
