@@ -50,32 +50,34 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 }
 
 // ---------------------------------------------------------------- k_stats
-// One CTA per head; each thread owns 4 channels (one 8-byte load per token)
-// and a strided subset of the tokens.  An fp16 value is X = M * 2^E (times
-// 2^-24) with M < 2^11, so X^2 = M^2 << 2E is one 32-bit multiply whose
-// shifted value spans two 32-bit limbs of a 128-bit sum, added with one
-// carry chain.  Integer sums are order-free, so the reduction order does
-// not matter for the result.
+// One CTA per head; each thread owns 4 channels and sums a strided subset of
+// the tokens.  An fp16 value is X = M * 2^E (times 2^-24) with M < 2^11 and
+// E <= 30, so X < 2^41; a 32-entry table gives 2^E and M's implicit bit for
+// each exponent field.  Most of the work is 32x32->64 multiply-adds, which
+// run on the FMA pipe beside the integer ALU:
+//   sum X    += (+-M) * 2^E                      (signed, 64-bit)
+//   X = a 2^21 + b (a < 2^20, b < 2^21):
+//   sum X^2  = 2^42 sum a^2 + 2^21 sum 2ab + sum b^2
+// Each of the three partial sums takes terms below 2^42, so 2^18 tokens
+// per thread (S <= 2^22) keep it below 2^60.  Integer sums are
+// order-free, so the reduction order does not matter for the result.
 constexpr int kStatsThreads = 512;
 
-__device__ __forceinline__ void acc_moments(uint32_t h, int64_t &T, uint32_t (&q)[4]) {
-  const uint32_t e = (h >> 10) & 31u;
-  const uint32_t M = e ? ((h & 1023u) | 1024u) : (h & 1023u);
-  const uint32_t E = e ? e - 1 : 0;  // X = M << E
-  const int64_t X = int64_t(uint64_t(M) << E);
-  T += (h & 0x8000u) ? -X : X;
-  const uint32_t m2 = M * M;     // < 2^22
-  const uint32_t sh = 2 * E;     // 0..60: m2 << sh lies in limbs sh/32 and sh/32 + 1
-  const uint32_t a = m2 << (sh & 31u);
-  const uint32_t b = __funnelshift_l(m2, 0u, sh & 31u);  // the bits shifted out of a
-  const bool up = sh >= 32;
-  const uint32_t v0 = up ? 0u : a, v1 = up ? a : b, v2 = up ? b : 0u;
-  asm("add.cc.u32 %0, %0, %4;\n\t"
-      "addc.cc.u32 %1, %1, %5;\n\t"
-      "addc.cc.u32 %2, %2, %6;\n\t"
-      "addc.u32 %3, %3, 0;"
-      : "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3])
-      : "r"(v0), "r"(v1), "r"(v2));
+struct Moments {
+  int64_t T;
+  uint64_t A2, AB, B2;
+};
+
+__device__ __forceinline__ void acc_moments(uint32_t h, const uint2 *ptab, Moments &m) {
+  const uint2 pe = ptab[(h >> 10) & 31u];  // (2^E, the implicit bit of M)
+  const uint32_t M = (h & 1023u) | pe.y;
+  const uint64_t X = uint64_t(M) * pe.x;
+  const int32_t sM = (h & 0x8000u) ? -int32_t(M) : int32_t(M);
+  m.T += int64_t(sM) * int32_t(pe.x);
+  const uint32_t a = uint32_t(X >> 21), b = uint32_t(X) & 0x1FFFFFu;
+  m.A2 += uint64_t(a) * a;
+  m.AB += uint64_t(a) * (2u * b);
+  m.B2 += uint64_t(b) * b;
 }
 
 // The head's rows stream through shared memory in 16 KB tiles, four in
@@ -108,7 +110,12 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
         const float *__restrict__ mult, Bases bases, uint32_t *status) {
   extern __shared__ __align__(128) unsigned char smem[];  // kStatsStages tiles, then the reduction
   __shared__ __align__(8) uint64_t bars[kStatsStages];
+  __shared__ uint2 ptab[32];  // per exponent field e: (2^max(e-1, 0), e ? 1024 : 0)
   __shared__ int s_timeout;
+  if (threadIdx.x < 32) {
+    const uint32_t e = threadIdx.x;
+    ptab[e] = make_uint2(e ? 1u << (e - 1) : 1u, e ? 1024u : 0u);
+  }
   const int si = blockIdx.x;
   const int tpr = lo.d / 4;                 // threads per token row
   const int rows = kStatsThreads / tpr;     // token rows summed side by side
@@ -139,13 +146,9 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   }
   __syncthreads();
 
-  int64_t T[4];
-  uint32_t Q[4][4];
+  Moments mo[4];
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    T[i] = 0;
-    Q[i][0] = Q[i][1] = Q[i][2] = Q[i][3] = 0;
-  }
+  for (int i = 0; i < 4; i++) mo[i] = Moments{0, 0, 0, 0};
   uint32_t bad = 0;  // bit 15 of a half: an all-ones exponent (Inf or NaN) was seen
   uint64_t t = 0;
   for (; t < ntiles; t++) {
@@ -161,7 +164,7 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
       const uint32_t hw[4] = {vv.x & 0xFFFFu, vv.x >> 16, vv.y & 0xFFFFu, vv.y >> 16};
       bad |= ((vv.x & 0x7C007C00u) + 0x04000400u) | ((vv.y & 0x7C007C00u) + 0x04000400u);
 #pragma unroll
-      for (int i = 0; i < 4; i++) acc_moments(hw[i], T[i], Q[i]);  // a non-finite value only spoils a flagged result
+      for (int i = 0; i < 4; i++) acc_moments(hw[i], ptab, mo[i]);  // a non-finite value only spoils a flagged result
     }
     __syncthreads();  // the stage has been read: it can take the next tile
     if (threadIdx.x == 0 && t + kStatsStages < ntiles) issue(t + kStatsStages);
@@ -176,15 +179,17 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   }
   if (bad & 0x80008000u) atomicOr(status, kStNonfinite);
 
-  int64_t *sT = reinterpret_cast<int64_t *>(smem);          // [rows][d]
-  uint64_t *sQl = reinterpret_cast<uint64_t *>(sT + rows * lo.d);
-  uint64_t *sQh = sQl + rows * lo.d;
+  int64_t *sT = reinterpret_cast<int64_t *>(smem);  // [rows][d] each
+  uint64_t *sA2 = reinterpret_cast<uint64_t *>(sT + rows * lo.d);
+  uint64_t *sAB = sA2 + rows * lo.d;
+  uint64_t *sB2 = sAB + rows * lo.d;
 #pragma unroll
   for (int i = 0; i < 4; i++) {
-    const int c = 4 * col + i;
-    sT[row * lo.d + c] = T[i];
-    sQl[row * lo.d + c] = uint64_t(Q[i][0]) | (uint64_t(Q[i][1]) << 32);
-    sQh[row * lo.d + c] = uint64_t(Q[i][2]) | (uint64_t(Q[i][3]) << 32);
+    const int c = row * lo.d + 4 * col + i;
+    sT[c] = mo[i].T;
+    sA2[c] = mo[i].A2;
+    sAB[c] = mo[i].AB;
+    sB2[c] = mo[i].B2;
   }
   __syncthreads();
   if (threadIdx.x < lo.d) {
@@ -193,7 +198,8 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     unsigned __int128 Qs = 0;
     for (int r = 0; r < rows; r++) {
       Ts += sT[r * lo.d + c];
-      Qs += (unsigned __int128)sQl[r * lo.d + c] | ((unsigned __int128)sQh[r * lo.d + c] << 64);
+      Qs += ((unsigned __int128)sA2[r * lo.d + c] << 42) + ((unsigned __int128)sAB[r * lo.d + c] << 21) +
+            (unsigned __int128)sB2[r * lo.d + c];
     }
     unsigned __int128 aT = (unsigned __int128)(Ts < 0 ? -Ts : Ts);
     unsigned __int128 num = (unsigned __int128)(uint64_t)lo.S * Qs - aT * aT;
@@ -424,7 +430,7 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
 cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
                          Bases bases, uint32_t *status, cudaStream_t st) {
   const int rows = kStatsThreads / (lo.d / 4);
-  const size_t smem = std::max(size_t(kStatsStages) * kStatsTile, size_t(rows) * lo.d * 24);
+  const size_t smem = std::max(size_t(kStatsStages) * kStatsTile, size_t(rows) * lo.d * 32);
   cudaError_t e = cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   k_stats<<<lo.nstr, kStatsThreads, smem, st>>>(lo, kv, tables, mult, bases, status);
