@@ -305,11 +305,11 @@ k_anchor(Layout lo, const uint16_t *__restrict__ kv, float2 *__restrict__ scale_
 }
 
 // ---------------------------------------------------------------- k_hist
-// One CTA per (level, head).  Threads work on channel pairs; a team of d/2
-// threads takes one anchor group at a time: it rebuilds a_hat from the
-// chunk's scale, quantizes the group's deltas and counts the symbols into
-// a shared [d][257] histogram (the odd row stride spreads channels over
-// banks).  Then one warp per channel normalises its counts.
+// One CTA per (level, head).  A team of d/4 threads (four channels each)
+// takes one anchor group at a time: it rebuilds a_hat from the chunk's
+// scale, quantizes the group's deltas and counts the symbols into a shared
+// histogram of d rows of 257 counts.  Then one warp per channel normalises
+// its counts.
 constexpr int kHistThreads = 1024;
 
 __global__ void __launch_bounds__(kHistThreads)
@@ -321,46 +321,53 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
   for (int i = threadIdx.x; i < lo.d * 257; i += blockDim.x) hist[i] = 0;
   __syncthreads();
 
-  const int tpr = lo.d / 2, teams = kHistThreads / tpr;
+  // four channels per thread (one 8-byte load per token); channel 4 col + i
+  // counts into histogram row i * (d/4) + col, so with the odd row stride
+  // the threads of a warp counting the same symbol hit different banks
+  const int tpr = lo.d / 4, teams = kHistThreads / tpr;
   const int col = threadIdx.x % tpr, team = threadIdx.x / tpr;
-  const int c0 = 2 * col;
-  const float *recipv = reinterpret_cast<const float *>(tables + lo.tb_recip);
-  const uint64_t ti = tab_index(lo, lv, l, kvi, h * lo.d + c0);
-  const float r0 = recipv[ti], r1 = recipv[ti + 1];
-  const uint32_t *head = reinterpret_cast<const uint32_t *>(kv + uint64_t(si) * lo.S * lo.d + c0);
-  const int dw = lo.d / 2;  // u32 words per token row
+  const int c0 = 4 * col;
+  const float4 r4 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(tables + lo.tb_recip) +
+                                                       tab_index(lo, lv, l, kvi, h * lo.d + c0));
+  const float rc[4] = {r4.x, r4.y, r4.z, r4.w};
+  uint32_t *hrow[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) hrow[i] = hist + (i * tpr + col) * 257;
+  const uint2 *head = reinterpret_cast<const uint2 *>(kv + uint64_t(si) * lo.S * lo.d + c0);
   const int64_t n_groups = int64_t(lo.n_chunks - 1) * lo.ng_full + lo.ng_last;
-  const int R = lo.R;
+  const uint32_t R = uint32_t(lo.R);
 
   for (int64_t gi = team; gi < n_groups; gi += teams) {
     const int k = int(gi / lo.ng_full), g = int(gi % lo.ng_full);
     const int64_t t0 = int64_t(k) * lo.C;
     const int64_t ta = t0 + int64_t(g) * lo.G;
-    const int64_t te = min(ta + lo.G, t0 + chunk_ntok(lo, k));
-    const float2 sc0 = scale[(uint64_t(k) * lo.nstr + si) * lo.d + c0];
-    const float2 sc1 = scale[(uint64_t(k) * lo.nstr + si) * lo.d + c0 + 1];
-    uint32_t wa = __ldg(head + ta * dw);
-    float xa0 = __half2float(__ushort_as_half(uint16_t(wa & 0xFFFF)));
-    float xa1 = __half2float(__ushort_as_half(uint16_t(wa >> 16)));
-    int a0 = max(-127, min(127, __float2int_rn(__fmul_rn(xa0, sc0.y))));
-    int a1 = max(-127, min(127, __float2int_rn(__fmul_rn(xa1, sc1.y))));
-    const float ah0 = __fmul_rn(float(a0), sc0.x), ah1 = __fmul_rn(float(a1), sc1.x);
-    for (int64_t tb = ta + 1; tb < te; tb += 8) {  // 8 rows in flight
-      uint32_t ws8[8];
+    const int te = int(min(ta + lo.G, t0 + chunk_ntok(lo, k)) - ta);  // rows of the group
+    const float4 *sp = reinterpret_cast<const float4 *>(scale + (uint64_t(k) * lo.nstr + si) * lo.d + c0);
+    const float4 s01 = sp[0], s23 = sp[1];  // (s, 127/absmax) of the four channels
+    const float sc[4] = {s01.x, s01.z, s23.x, s23.z}, inv[4] = {s01.y, s01.w, s23.y, s23.w};
+    const uint2 *grow = head + ta * tpr;
+    const uint2 wa = __ldg(grow);
+    const uint32_t ha[4] = {wa.x & 0xFFFFu, wa.x >> 16, wa.y & 0xFFFFu, wa.y >> 16};
+    float ah[4];
 #pragma unroll
-      for (int u = 0; u < 8; u++) ws8[u] = (tb + u < te) ? __ldg(head + (tb + u) * dw) : 0u;
+    for (int i = 0; i < 4; i++) {
+      const int a = max(-127, min(127, __float2int_rn(__fmul_rn(__half2float(__ushort_as_half(uint16_t(ha[i]))), inv[i]))));
+      ah[i] = __fmul_rn(float(a), sc[i]);
+    }
+    for (int tb = 1; tb < te; tb += 8) {  // 8 rows in flight
+      uint2 w8[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) w8[u] = tb + u < te ? __ldg(grow + (tb + u) * tpr) : make_uint2(0, 0);
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         if (tb + u >= te) break;
-        const uint32_t w = ws8[u];
-        float x0 = __half2float(__ushort_as_half(uint16_t(w & 0xFFFF)));
-        float x1 = __half2float(__ushort_as_half(uint16_t(w >> 16)));
-        int q0 = __float2int_rn(__fmul_rn(__fsub_rn(x0, ah0), r0));
-        int q1 = __float2int_rn(__fmul_rn(__fsub_rn(x1, ah1), r1));
-        int s0 = (q0 >= -R && q0 <= R) ? q0 + 127 : kEsc;
-        int s1 = (q1 >= -R && q1 <= R) ? q1 + 127 : kEsc;
-        atomicAdd(&hist[c0 * 257 + s0], 1u);
-        atomicAdd(&hist[(c0 + 1) * 257 + s1], 1u);
+        const uint32_t hw[4] = {w8[u].x & 0xFFFFu, w8[u].x >> 16, w8[u].y & 0xFFFFu, w8[u].y >> 16};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const int q = __float2int_rn(__fmul_rn(__fsub_rn(__half2float(__ushort_as_half(uint16_t(hw[i]))), ah[i]), rc[i]));
+          const int sym = uint32_t(q) + R <= 2 * R ? q + 127 : kEsc;  // |q| <= R as one unsigned compare
+          atomicAdd(&hrow[i][sym], 1u);
+        }
       }
     }
   }
@@ -375,7 +382,7 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
     int bests = 8 * lane;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      n[i] = hist[c * 257 + 8 * lane + i];
+      n[i] = hist[((c & 3) * (lo.d / 4) + (c >> 2)) * 257 + 8 * lane + i];
       nsum += n[i];
       if (n[i] > best) { best = n[i]; bests = 8 * lane + i; }
     }
