@@ -192,17 +192,27 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
         // ring size, so a block of 256 words sits in the ring in the order it
         // takes at the end of the scratch slot (which is filled backwards)
         uint32_t e = uint32_t(E) + uint32_t(suf - cntw);
+        if (esc[0] | esc[1] | esc[2] | esc[3]) {  // escapes (rare): the raw q follows the word
 #pragma unroll
-        for (int j = 3; j >= 0; j--) {
-          if (esc[j]) {
-            ring[~e & (kWordRing - 1)] = uint16_t(qv[j] >> 16);
-            ring[~(e + 1) & (kWordRing - 1)] = uint16_t(qv[j] & 0xFFFFu);
-            e += 2;
-            nesc++;
+          for (int j = 3; j >= 0; j--) {
+            if (esc[j]) {
+              ring[~e & (kWordRing - 1)] = uint16_t(qv[j] >> 16);
+              ring[~(e + 1) & (kWordRing - 1)] = uint16_t(qv[j] & 0xFFFFu);
+              e += 2;
+              nesc++;
+            }
+            if (ren[j]) {
+              ring[~e & (kWordRing - 1)] = uint16_t(word[j]);
+              e += 1;
+            }
           }
-          if (ren[j]) {
-            ring[~e & (kWordRing - 1)] = uint16_t(word[j]);
-            e += 1;
+        } else {
+#pragma unroll
+          for (int j = 3; j >= 0; j--) {
+            if (ren[j]) {
+              ring[~e & (kWordRing - 1)] = uint16_t(word[j]);
+              e += 1;
+            }
           }
         }
         const uint32_t e0 = uint32_t(E), e1 = e0 + uint32_t(tot);
