@@ -124,15 +124,17 @@ def test_gpu_roundtrip_error_bound(orc):
 
 
 # ---------------------------------------------------------------- failures
-def _small(orc):
-    x, cd, cfg, levels, lb, lm = _setup(orc, "d8_group7")
+def _small(orc, name="d8_group7"):
+    x, cd, cfg, levels, lb, lm = _setup(orc, name)
     rc, tb = orc.fit_tables(cd, list(lb), lm, x)
-    rc, cont, _ = orc.encode(cd, 1, tb, x, levels)
+    rc, cont, _ = orc.encode(cd, len(lb), tb, x, levels)
     return x, cd, cfg, levels, tb, cont
 
 
-def test_corrupt_containers_flagged(orc):
-    x, cd, cfg, levels, tb, cont = _small(orc)
+# d = 8; d = 128 with 3 chunks (compact tables); d = 128 with 42 chunks (full tables)
+@pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams"])
+def test_corrupt_containers_flagged(orc, name):
+    x, cd, cfg, levels, tb, cont = _small(orc, name)
     assert gu.decode(cfg, tb, cont)[0] == cg.CG_OK
     bad = cont.copy()
     bad[0] ^= 1
@@ -157,10 +159,10 @@ def test_corrupt_containers_flagged(orc):
     b4[base + fixed_off: base + fixed_off + 4] = np.array([1 << 30], np.uint32).view(np.uint8)
     assert gu.decode(cfg, tb, b4)[0] == cg.CG_ERR_CORRUPT
     tb2 = tb.copy()  # a table whose CDF is not increasing
-    _, _, cdfv = orc.tables_views(tb2, cd, 1)
+    _, _, cdfv = orc.tables_views(tb2, cd, len(CASES[name][4]))
     cdfv[0, 0, 0, 0, 100] = cdfv[0, 0, 0, 0, 99]
     assert gu.decode(cfg, tb2, cont)[0] == cg.CG_ERR_CORRUPT
-    other = cg.Config(cd.L, cd.H, cd.d, cd.S, cd.C, G=cd.G + 1, R=cd.R, level_base=(0.2,))
+    other = cg.Config(cd.L, cd.H, cd.d, cd.S, cd.C, G=cd.G + 1, R=cd.R, level_base=CASES[name][4])
     assert gu.decode(other, tb, cont)[0] == cg.CG_ERR_CORRUPT                  # dims mismatch
 
 
