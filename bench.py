@@ -355,32 +355,49 @@ def main():
     for ws, what in ((ws_fit, "fit"), (ws_enc, "encode"), (ws_dec, "decode")):
         cg.check(cg.cg_read_status(ws), what)
 
-    # end to end through host buffers: the container's H2D copy, then the
-    # decode in layer groups, each group's KV copied back to the host on a
-    # copy stream while the next group decodes (a user's pattern with
-    # cg_decode_layers); the plain serial sequence is timed beside it
+    # end to end through host buffers, pipelined by chunk group (4 chunks):
+    # the group's container bytes go to the device on one stream, the group
+    # decodes on another (cg_decode with a chunk range), and its tokens come
+    # back on a third (one strided copy: a run of the group's tokens from
+    # every (layer, K/V, head) row); the serial sequence (container H2D, one
+    # cg_decode, KV D2H) is timed beside it
+    import ctypes
+    import glob
     cont_host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     cont_host.copy_(out[:nbytes])
     out_host = torch.empty(kv.numel(), dtype=torch.int16, pin_memory=True)
     cont_dev = cg.empty_u8(nbytes)
-    per_layer = kv.numel() // w.L
-    e2e_groups = [(l0, min(l0 + 19, w.L)) for l0 in range(0, w.L, 19)]
-    copy_streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    offs = [int(v) for v in cont_host[64:64 + 8 * w.n_chunks].numpy().view(np.uint64)] + [nbytes]
+    cudart = ctypes.CDLL(sorted(glob.glob(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
+                                                       "lib64", "libcudart.so.*")))[-1])
+    cudart.cudaMemcpy2DAsync.restype = ctypes.c_int
+    cudart.cudaMemcpy2DAsync.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    e2e_groups = [(k0, min(k0 + 4, w.n_chunks)) for k0 in range(0, w.n_chunks, 4)]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    row_bytes = w.S * w.d * 2
     torch.cuda.synchronize()
 
     def e2e_pipelined():
-        cont_dev.copy_(cont_host, non_blocking=True)
-        for gi, (l0, l1) in enumerate(e2e_groups):
-            cg.check(cg.cg_decode_layers(cfg, tables, cont_dev, nbytes, 0, -1, l0, l1, kv_out, ws_dec, stream),
-                     "cg_decode_layers")
-            done = torch.cuda.Event()
-            done.record(stream)
-            cs = copy_streams[gi % 2]
-            cs.wait_event(done)
-            with torch.cuda.stream(cs):
-                out_host[l0 * per_layer:l1 * per_layer].copy_(kv_out[l0 * per_layer:l1 * per_layer], non_blocking=True)
-        for cs in copy_streams:
-            stream.wait_stream(cs)
+        h2d_s.wait_stream(stream)  # the copies start inside the timed region
+        for k0, k1 in e2e_groups:
+            lo_b = 0 if k0 == 0 else offs[k0]  # the first group carries the header and chunk index
+            with torch.cuda.stream(h2d_s):
+                cont_dev[lo_b:offs[k1]].copy_(cont_host[lo_b:offs[k1]], non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(h2d_s)
+            stream.wait_event(arrived)
+            cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, k0, k1, kv_out, ws_dec, stream), "cg_decode")
+            decoded = torch.cuda.Event()
+            decoded.record(stream)
+            d2h_s.wait_event(decoded)
+            t0_, t1_ = k0 * w.C, min(k1 * w.C, w.S)
+            off = t0_ * w.d * 2
+            rc = cudart.cudaMemcpy2DAsync(out_host.data_ptr() + off, row_bytes, kv_out.data_ptr() + off, row_bytes,
+                                          (t1_ - t0_) * w.d * 2, w.L * 2 * w.H, 2, ctypes.c_void_p(d2h_s.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"cudaMemcpy2DAsync failed ({rc})")
+        stream.wait_stream(d2h_s)
 
     def e2e_serial():
         cont_dev.copy_(cont_host, non_blocking=True)
@@ -567,8 +584,8 @@ def main():
                             "algorithmic_bytes_per_launch": enc_alg},
         "e2e": {"value": job_gbs(fp16, world, ms_e2e), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
                 "d2h_bytes_per_step": fp16,
-                "what": "pinned-host container -> cg_decode_layers in 19-layer groups, each group's KV copied "
-                        "back to pinned host memory while the next decodes",
+                "what": "pinned-host container -> cg_decode by 4-chunk group -> pinned-host KV; each group's "
+                        "copy in, decode and copy out overlap the neighbouring groups'",
                 "serial": {"value": job_gbs(fp16, world, ms_e2e_serial), "unit": "GB/s",
                            "what": "container H2D, one cg_decode, KV D2H, in sequence"}},
         "decode_paged": paged,
