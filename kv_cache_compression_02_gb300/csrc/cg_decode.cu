@@ -343,30 +343,30 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     uint16_t *orow;
     bool row_ok = true, bad_row = false;
     [[maybe_unused]] uint16_t *pool = nullptr;
-    [[maybe_unused]] int64_t lblk = 0, n_lblk = 0;
-    [[maybe_unused]] int tib = 0, tl = 0;
-    [[maybe_unused]] int32_t bnext = 0;  // block id of logical block lblk + 1, loaded a block ahead
+    [[maybe_unused]] int64_t lblk = 0, lblk_end = 0;  // logical block; one past the chunk's last
+    [[maybe_unused]] int left = 0;                    // rows left in the current block
+    [[maybe_unused]] int32_t bnext = 0;               // block id of logical block lblk + 1, loaded a block ahead
     if constexpr (PAGED) {
       pool = po.pools[l * 2 + kvi];
       const int64_t t0 = int64_t(k) * lo.C;
-      n_lblk = (lo.S + po.bt - 1) / po.bt;
       lblk = t0 / po.bt;
-      tib = int(t0 - lblk * po.bt);
+      lblk_end = (t0 + ntok - 1) / po.bt + 1;
+      const int tib = int(t0 - lblk * po.bt);
+      left = po.bt - tib;
       orow = paged_row(po, pool, po.table[lblk], tib, h, lo, i, row_ok);
-      if (lblk + 1 < n_lblk) bnext = po.table[lblk + 1];
+      bad_row = !row_ok;
+      if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
     } else {
       orow = kv + (uint64_t(si) * lo.S + uint64_t(k) * lo.C) * lo.d + kLpt * i;
     }
     auto next_row = [&]() {
       if constexpr (PAGED) {
-        bad_row |= !row_ok;
-        ++tl;
-        if (++tib == po.bt) {  // next block, if the chunk has another token
-          tib = 0;
-          ++lblk;
-          if (tl < ntok) {
+        if (--left == 0) {  // the block is full: the next one, if the chunk reaches it
+          left = po.bt;
+          if (++lblk < lblk_end) {
             orow = paged_row(po, pool, bnext, 0, h, lo, i, row_ok);
-            if (lblk + 1 < n_lblk) bnext = po.table[lblk + 1];
+            bad_row |= !row_ok;
+            if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
           }
         } else {
           orow += lo.d;
