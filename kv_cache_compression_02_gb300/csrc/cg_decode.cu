@@ -421,12 +421,51 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
           }
           sl[j] = rr[j] >= ff[j];
         }
-        // Slow lanes (well under 1%): a binary search in the lane's own table
-        // column, between the previous bucket's pair and the chosen pair when
-        // the slot is below it, else between the pair and the next bucket's
-        // pair; symbol 255 is the escape, whose raw value follows in the words.
+        // Slow lanes: about 1% of lanes (more with the compact tables' wider
+        // buckets).  Symbol 255 is the escape, whose raw value follows in the
+        // words.
         uint32_t escm = 0;
-        if (sl[0] | sl[1] | sl[2] | sl[3]) {
+        if constexpr (T == 32 && COMPACT) {
+          // Compact tables: the whole warp resolves a slow lane at a time.
+          // The owner's slot goes to every thread; thread r reads row 8r of
+          // the owner's cdf column, and since the rows increase, one ballot
+          // counts the rows at or below the slot and so fixes its group of
+          // 8 symbols; a second ballot over the group's rows (and the next
+          // row, for the frequency) gives the symbol.  No thread diverges.
+          // (With the full tables' narrower buckets, most slow lanes sit one
+          // or two symbols from the pair and the per-lane binary search below
+          // is cheaper.)
+          if (__any_sync(0xffffffffu, sl[0] | sl[1] | sl[2] | sl[3])) {
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              const int cj = (j >> 1) * T * 2 + (j & 1);
+              const uint32_t slot = x[j] & 0xFFFFu;
+              for (uint32_t m = __ballot_sync(0xffffffffu, sl[j]); m; m &= m - 1) {
+                const int t = __ffs(m) - 1;
+                const uint32_t st = __shfl_sync(0xffffffffu, slot, t);
+                const int col = 2 * t + cj;  // the owner's column within a cdf row
+                const uint32_t cr8 = cdfc[(8 * uint32_t(i)) * kRow + col];
+                const uint32_t g = 8 * (__popc(__ballot_sync(0xffffffffu, cr8 <= st)) - 1);  // cdf_0 = 0
+                const uint32_t r = g + uint32_t(i);
+                const bool win = i < 9 && r <= 255u;
+                const uint32_t crow = cdfc[(win ? r : g) * kRow + col];
+                const uint32_t c = __popc(__ballot_sync(0xffffffffu, win && i < 8 && crow <= st));  // >= 1
+                const uint32_t s = g + c - 1;
+                const uint32_t c0 = __shfl_sync(0xffffffffu, crow, (c - 1) & 31);
+                const uint32_t c1 = __shfl_sync(0xffffffffu, crow, c & 31);
+                if (i == t) {
+                  sy[j] = s;
+                  ff[j] = (s < 255 ? c1 : kM) - c0;
+                  rr[j] = st - c0;
+                  escm |= s == uint32_t(kEsc) ? (1u << j) : 0u;
+                }
+              }
+            }
+          }
+        } else if (sl[0] | sl[1] | sl[2] | sl[3]) {
+          // a binary search in the lane's own table column, between the
+          // previous bucket's pair and the chosen pair when the slot is below
+          // it, else between the pair and the next bucket's pair
 #pragma unroll
           for (int j = 0; j < 4; j++) {
             if (sl[j]) {
