@@ -169,6 +169,14 @@ cg_status cg_assemble(const cg_dims *dims, const cg_params *params, const void *
  * container header).  The container must be bitstream_bytes long and the
  * caller must keep it and the tables alive until the stream reaches the
  * decode.  ws_dev: cg_workspace_bytes(CG_OP_DECODE) bytes.
+ * Host-resident buffers: bitstream_dev and kv_dev (here and in
+ * cg_decode_layers) may be pinned host memory mapped into the device's
+ * address space (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped), passed as the device address
+ * cudaHostGetDevicePointer returns.  The decoder then reads the container
+ * and writes the tokens across the host link itself, with no staging copy
+ * (the receiver of a streamed context decodes as the bytes arrive: Guide to
+ * CacheGen, pillar 4).  Tables and workspace stay in device memory.
  * Device errors: CG_ERR_CORRUPT (header/offset/table mismatch, a stream
  * whose lanes do not end in the initial state, or whose word or escape
  * count disagrees with its header); decoding never reads outside the
