@@ -437,6 +437,22 @@ def main():
         if not torch.equal(out_host[lo_:lo_ + (1 << 24)], kv_out[lo_:lo_ + (1 << 24)].cpu()):
             raise RuntimeError("end-to-end copy differs from the decoded KV")
     cg.check(cg.cg_read_status(ws_dec), "decode (e2e)")
+    # the host link alone, by the copy engines, on the same buffers: the
+    # bound the end-to-end decode is measured against
+    link = {}
+    for name, fn, nb_ in (("h2d_gbs", lambda: cont_dev.copy_(cont_host, non_blocking=True), nbytes),
+                          ("d2h_gbs", lambda: out_host.copy_(kv_out, non_blocking=True), kv.numel() * 2)):
+        ts = []
+        for i in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i:
+                ts.append(a.elapsed_time(b))
+        link[name] = nb_ / (statistics.mean(ts) * 1e-3) / 1e9
 
     # the same decode in layer groups, in execution order: 19 layers (304
     # CTAs, two full waves) per launch, an event after each group
@@ -604,6 +620,8 @@ def main():
                 "d2h_bytes_per_step": fp16,
                 "what": "one cg_decode from a pinned-host container into a pinned-host KV buffer, both mapped "
                         "into the device address space: the decoder reads and writes across the host link",
+                "link": dict(link, what="copy-engine rates of the same buffers alone (container in, KV out)",
+                             frac_of_d2h_bound=(fp16 / (link["d2h_gbs"] * 1e9)) / (ms_e2e * 1e-3)),
                 "pipelined": {"value": job_gbs(fp16, world, ms_e2e_pipe), "unit": "GB/s",
                               "what": "per 4-chunk group: container H2D, cg_decode of the group, strided KV D2H, "
                                       "overlapped with the neighbouring groups on three streams"},

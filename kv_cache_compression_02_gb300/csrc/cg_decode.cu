@@ -55,8 +55,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Words staged per team: a ring of kRing words in two halves.
-constexpr uint32_t kRing = 512, kHalf = 256;
+// Words staged per team: a ring of kRing words in two halves, followed by
+// a copy of its first kMirror words, so that a thread's (up to four) words
+// can be read from one base index without wrapping.
+constexpr uint32_t kRing = 512, kHalf = 256, kMirror = 16;
+// (compact tables read word by word and keep no mirror)
+template <bool COMPACT>
+__host__ __device__ constexpr uint32_t ring_stride() { return COMPACT ? kRing : kRing + kMirror; }
 // Symbol-search buckets: slot >> kBucketShift, kBuckets of them.
 constexpr uint32_t kBucketShift = 7, kBuckets = 1u << (16 - kBucketShift), kBucketSlots = 1u << kBucketShift;
 constexpr uint32_t kCdfRows = 258;  // cdf_0 .. cdf_255, cdf_255 again, padding
@@ -130,7 +135,8 @@ __device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *poo
 //                                          pair holding most of the bucket
 //   cdfc  [258 rows][4 lanes x T] u16    : cdf_s for s < 256; row 256 repeats
 //                                          cdf_255; row 257 is padding
-//   rings [teams][512] u16               : the staged words of each team
+//   rings [teams][512 + 16] u16          : the staged words of each team
+//                                          (512 with the compact tables)
 // Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
 // access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
@@ -154,7 +160,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   uint8_t *lut8 = reinterpret_cast<uint8_t *>(smem);               // COMPACT: [kCBuckets][T][4]
   uint16_t *cdfc = COMPACT ? reinterpret_cast<uint16_t *>(lut8 + kCBuckets * kLpt * T)
                            : lut16 + kBuckets * kLpt * T;              // [kCdfRows][2][T][2]
-  uint16_t *rings = cdfc + kCdfRows * kLpt * T;                      // [teams][kRing] words
+  uint16_t *rings = cdfc + kCdfRows * kLpt * T;                      // [teams][ring_stride] words
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
@@ -317,13 +323,18 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     uint32_t x[4] = {xs.x, xs.y, xs.z, xs.w};
     const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
     // stage the first kRing words (two halves) of the stream in the ring
-    uint16_t *ring = rings + team * kRing;
+    uint16_t *ring = rings + team * ring_stride<COMPACT>();
     const uint32_t wbytes = 2 * nw;
     auto load_half = [&](uint32_t w0) {  // words [w0, w0 + kHalf) -> ring half
       for (uint32_t o = 16 * i; o < 2 * kHalf; o += 16 * T) {
         const uint32_t b = 2 * w0 + o;  // byte offset in the word array
         const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
         cp_async16(ring + ((w0 + o / 2) & (kRing - 1)), reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
+      }
+      if (!COMPACT && (w0 & (kRing - 1)) == 0 && 16 * uint32_t(i) < 2 * kMirror) {  // the mirror of ring[0, kMirror)
+        const uint32_t b = 2 * w0 + 16 * i;
+        const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
+        cp_async16(ring + kRing + 8 * i, reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
       }
       cp_async_commit();
     };
@@ -564,17 +575,34 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         float v[4];
         if (in_ring) {
         if (escm == 0) {
+          if constexpr (COMPACT) {  // thin launches: per-lane reads (the shorter dependency chain pays)
 #pragma unroll
-          for (int j = 0; j < 4; j++) {
-            {
-              const uint32_t w = ring[pos & (kRing - 1)];  // read unconditionally, use if needed
-              const bool nd = nd4[j];
-              x[j] = nd ? __byte_perm(w, x[j], 0x5410) : x[j];  // x<<16 | w
-              pos += nd ? 1u : 0u;
+            for (int j = 0; j < 4; j++) {
+              {
+                const uint32_t w = ring[pos & (kRing - 1)];  // read unconditionally, use if needed
+                const bool nd = nd4[j];
+                x[j] = nd ? __byte_perm(w, x[j], 0x5410) : x[j];  // x<<16 | w
+                pos += nd ? 1u : 0u;
+              }
+              // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
+              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+              v[j] = __fmaf_rn(qf, step[j], ah[j]);
             }
-            // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
-            const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
-            v[j] = __fmaf_rn(qf, step[j], ah[j]);
+          } else {
+            // the thread's words are consecutive from pos: read four (the
+            // mirror covers reads past the ring's end; unneeded ones are
+            // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
+            const uint16_t *rp = ring + (pos & (kRing - 1));
+            const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3];
+            const uint32_t a1 = nd4[0] ? w1 : w0, a2 = nd4[0] ? w2 : w1, a3 = nd4[0] ? w3 : w2;
+            const uint32_t b2 = nd4[1] ? a2 : a1, b3 = nd4[1] ? a3 : a2;
+            const uint32_t wl[4] = {w0, a1, b2, nd4[2] ? b3 : b2};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              x[j] = nd4[j] ? __byte_perm(wl[j], x[j], 0x5410) : x[j];  // x<<16 | w
+              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;  // as above
+              v[j] = __fmaf_rn(qf, step[j], ah[j]);
+            }
           }
         } else {  // escapes: the raw q follows the lane's renormalisation word
 #pragma unroll
@@ -634,7 +662,7 @@ cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uin
                               uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po, int l0, int l1) {
   const size_t tabs = COMPACT ? size_t(kCBuckets) * lo.d + size_t(kCdfRows) * lo.d * 2
                               : size_t(kBuckets + kCdfRows) * lo.d * 2;
-  const size_t smem = tabs + size_t(teams) * kRing * 2;
+  const size_t smem = tabs + size_t(teams) * ring_stride<COMPACT>() * 2;
   cudaError_t e =
       cudaFuncSetAttribute(k_decode<T, PAGED, COMPACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two compact CTAs fit
