@@ -127,7 +127,7 @@ __device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *poo
 }
 
 // ---------------------------------------------------------------- decode
-// Shared memory per CTA (d lanes, T = d/4 threads per team), 217 KB at d=128
+// Shared memory per CTA (d lanes, T = d/4 threads per team), 215 KB at d=128
 // with 22 teams:
 //   lut16 [512 buckets][4 lanes x T] u16 : sa << 8 | (255 - last offset of sa
 //                                          in the 128-slot bucket), where
