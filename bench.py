@@ -373,17 +373,7 @@ def main():
     cudart = ctypes.CDLL(sorted(glob.glob(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
                                                        "lib64", "libcudart.so.*")))[-1])
     cudart.cudaMemcpy2DAsync.restype = ctypes.c_int
-    cudart.cudaHostGetDevicePointer.restype = ctypes.c_int
-    cudart.cudaHostGetDevicePointer.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
-
-    def mapped(t):  # the device address of a pinned host tensor
-        dp = ctypes.c_void_p(0)
-        rc = cudart.cudaHostGetDevicePointer(ctypes.byref(dp), ctypes.c_void_p(t.data_ptr()), 0)
-        if rc != 0 or not dp.value:
-            raise RuntimeError(f"pinned host buffer is not mapped into the device address space ({rc})")
-        return dp.value
-
-    cont_map, out_map = mapped(cont_host), mapped(out_host)
+    cont_map, out_map = cg.cg_host_mapped(cont_host), cg.cg_host_mapped(out_host)
     cudart.cudaMemcpy2DAsync.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
     e2e_groups = [(k0, min(k0 + 4, w.n_chunks)) for k0 in range(0, w.n_chunks, 4)]

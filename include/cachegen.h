@@ -172,8 +172,8 @@ cg_status cg_assemble(const cg_dims *dims, const cg_params *params, const void *
  * Host-resident buffers: bitstream_dev and kv_dev (here and in
  * cg_decode_layers) may be pinned host memory mapped into the device's
  * address space (cudaHostAlloc, or cudaHostRegister with
- * cudaHostRegisterMapped), passed as the device address
- * cudaHostGetDevicePointer returns.  The decoder then reads the container
+ * cudaHostRegisterMapped), passed as the device address cg_host_mapped
+ * returns.  The decoder then reads the container
  * and writes the tokens across the host link itself, with no staging copy
  * (the receiver of a streamed context decodes as the bytes arrive: Guide to
  * CacheGen, pillar 4).  Tables and workspace stay in device memory.
@@ -292,6 +292,14 @@ cg_status cg_simulate_stream(int32_t n_chunks, int32_t n_levels, const uint64_t 
 /* Status of the last call that used this workspace (blocking read of the
  * device status word; synchronise the call's stream first). */
 cg_status cg_read_status(const void *ws_dev);
+
+/* The device address of host memory that is pinned and mapped into the
+ * device's address space (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped), for the host-resident decode described at
+ * cg_decode.  *dev_ptr receives it (NULL on error).  Errors:
+ * CG_ERR_INVALID_ARG when host_ptr is not in such memory or a pointer is
+ * NULL.  Host only; it launches nothing. */
+cg_status cg_host_mapped(const void *host_ptr, void **dev_ptr);
 
 /* Human-readable name of a status code (static string). */
 const char *cg_status_str(cg_status status);

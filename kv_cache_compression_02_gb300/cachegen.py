@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "cg_decode": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                          P, P, S, P]),
             "cg_read_status": (ctypes.c_int, [P]),
+            "cg_host_mapped": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_void_p)]),
             "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                  P, P, ctypes.POINTER(ctypes.c_void_p)]),
             "cg_assemble": (ctypes.c_int, [D, Pr, P, P, P, P, ctypes.c_uint64, P, P, S, P]),
@@ -249,6 +250,15 @@ def cg_simulate_stream(chunk_bytes, trace, levels, decode_s):
 
 def cg_read_status(ws) -> int:
     return lib().cg_read_status(_ptr(ws))
+
+
+def cg_host_mapped(t) -> int:
+    """The device address of a pinned, mapped host tensor (or address), to
+    pass as a container or output of the decode calls.  Raises
+    CacheGenError when the memory is not pinned and mapped."""
+    dp = ctypes.c_void_p(0)
+    check(lib().cg_host_mapped(_ptr(t), ctypes.byref(dp)), "cg_host_mapped")
+    return int(dp.value)
 
 
 # ---- buffer helpers (torch allocates; nothing here computes) ----------------

@@ -224,4 +224,17 @@ cg_status cg_read_status(const void *ws_dev) {
   return CG_OK;
 }
 
+cg_status cg_host_mapped(const void *host_ptr, void **dev_ptr) {
+  if (!dev_ptr) return CG_ERR_INVALID_ARG;
+  *dev_ptr = nullptr;
+  if (!host_ptr) return CG_ERR_INVALID_ARG;
+  void *d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void *>(host_ptr), 0) != cudaSuccess || !d) {
+    (void)cudaGetLastError();  // not pinned, mapped host memory: an argument error, not a sticky one
+    return CG_ERR_INVALID_ARG;
+  }
+  *dev_ptr = d;
+  return CG_OK;
+}
+
 }  // extern "C"

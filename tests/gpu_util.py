@@ -73,15 +73,5 @@ def decode(cfg: cg.Config, tables: np.ndarray, cont: np.ndarray, k0=0, k1=-1, nb
 
 
 def host_mapped(t) -> int:
-    """The device address of a pinned host tensor (cudaHostGetDevicePointer)."""
-    import ctypes
-    import glob
-    import os
-    libs = sorted(glob.glob(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcudart.so.*")))
-    rt = ctypes.CDLL(libs[-1])
-    rt.cudaHostGetDevicePointer.restype = ctypes.c_int
-    rt.cudaHostGetDevicePointer.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
-    dp = ctypes.c_void_p(0)
-    rc = rt.cudaHostGetDevicePointer(ctypes.byref(dp), ctypes.c_void_p(t.data_ptr()), 0)
-    assert rc == 0 and dp.value, f"pinned buffer not mapped ({rc})"
-    return dp.value
+    """The device address of a pinned host tensor (the library's cg_host_mapped)."""
+    return cg.cg_host_mapped(t)

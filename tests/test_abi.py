@@ -82,6 +82,10 @@ def test_invalid_arguments(lib):
     cfg = cg.Config(L=1, H=1, d=8, S=10, C=10)
     assert cg.cg_workspace_bytes(cfg, 7) == 0
     assert lib.cg_fit_tables(None, None, None, None, None, 0, None) == cg.CG_ERR_INVALID_ARG
+    # cg_host_mapped: null pointers are rejected before any CUDA call, and the output is cleared
+    dp = ctypes.c_void_p(123)
+    assert lib.cg_host_mapped(None, ctypes.byref(dp)) == cg.CG_ERR_INVALID_ARG and not dp.value
+    assert lib.cg_host_mapped(ctypes.c_void_p(1 << 20), None) == cg.CG_ERR_INVALID_ARG
     # cg_decode_paged: missing pointers or a block size below 1, rejected before any CUDA call
     ok = cg.Config(L=1, H=1, d=8, S=10, C=10)
     fake = 1 << 20  # an aligned non-null address that is never dereferenced

@@ -74,6 +74,13 @@ def test_chunk_range_host_to_host_writes_only_its_tokens(orc, case):
     assert np.array_equal(_run(case, 4, 7), want)
 
 
+def test_mapped_address_of_device_memory_is_refused(case):
+    T = gu.torch()
+    gu.ready()
+    with pytest.raises(cg.CacheGenError):
+        cg.cg_host_mapped(T.empty(64, dtype=T.uint8, device="cuda"))
+
+
 def test_layer_range_host_to_host(orc, case):
     spec, cfg, tb, cont = case
     rc, ref = orc.decode(tb, cont)
