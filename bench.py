@@ -373,9 +373,9 @@ def main():
     cudart = ctypes.CDLL(sorted(glob.glob(os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
                                                        "lib64", "libcudart.so.*")))[-1])
     cudart.cudaMemcpy2DAsync.restype = ctypes.c_int
-    cont_map, out_map = cg.cg_host_mapped(cont_host), cg.cg_host_mapped(out_host)
     cudart.cudaMemcpy2DAsync.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    cont_map, out_map = cg.cg_host_mapped(cont_host), cg.cg_host_mapped(out_host)  # for the direct decode
     e2e_groups = [(k0, min(k0 + 4, w.n_chunks)) for k0 in range(0, w.n_chunks, 4)]
     h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     row_bytes = w.S * w.d * 2
