@@ -297,8 +297,9 @@ cg_status cg_read_status(const void *ws_dev);
  * device's address space (cudaHostAlloc, or cudaHostRegister with
  * cudaHostRegisterMapped), for the host-resident decode described at
  * cg_decode.  *dev_ptr receives it (NULL on error).  Errors:
- * CG_ERR_INVALID_ARG when host_ptr is not in such memory or a pointer is
- * NULL.  Host only; it launches nothing. */
+ * CG_ERR_INVALID_ARG when host_ptr is not in page-locked host memory
+ * (device, managed and pageable memory are refused) or a pointer is NULL.
+ * Host only; it launches nothing. */
 cg_status cg_host_mapped(const void *host_ptr, void **dev_ptr);
 
 /* Human-readable name of a status code (static string). */

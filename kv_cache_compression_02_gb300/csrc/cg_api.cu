@@ -228,9 +228,14 @@ cg_status cg_host_mapped(const void *host_ptr, void **dev_ptr) {
   if (!dev_ptr) return CG_ERR_INVALID_ARG;
   *dev_ptr = nullptr;
   if (!host_ptr) return CG_ERR_INVALID_ARG;
+  // only page-locked host memory qualifies (device, managed and ordinary
+  // pageable memory are refused); its device address may differ from the
+  // host one where the platform has no unified addressing
+  cudaPointerAttributes a{};
   void *d = nullptr;
-  if (cudaHostGetDevicePointer(&d, const_cast<void *>(host_ptr), 0) != cudaSuccess || !d) {
-    (void)cudaGetLastError();  // not pinned, mapped host memory: an argument error, not a sticky one
+  if (cudaPointerGetAttributes(&a, host_ptr) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&d, const_cast<void *>(host_ptr), 0) != cudaSuccess || !d) {
+    (void)cudaGetLastError();  // an argument error, not a sticky one
     return CG_ERR_INVALID_ARG;
   }
   *dev_ptr = d;

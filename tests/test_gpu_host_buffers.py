@@ -74,11 +74,14 @@ def test_chunk_range_host_to_host_writes_only_its_tokens(orc, case):
     assert np.array_equal(_run(case, 4, 7), want)
 
 
-def test_mapped_address_of_device_memory_is_refused(case):
+def test_mapped_address_only_for_page_locked_host_memory(case):
     T = gu.torch()
     gu.ready()
-    with pytest.raises(cg.CacheGenError):
-        cg.cg_host_mapped(T.empty(64, dtype=T.uint8, device="cuda"))
+    pinned = T.empty(64, dtype=T.uint8, pin_memory=True)
+    assert cg.cg_host_mapped(pinned) != 0
+    for t in (T.empty(64, dtype=T.uint8, device="cuda"), T.empty(64, dtype=T.uint8)):  # device, pageable
+        with pytest.raises(cg.CacheGenError):
+            cg.cg_host_mapped(t)
 
 
 def test_layer_range_host_to_host(orc, case):
