@@ -283,7 +283,7 @@ def run_reference(args):
     w = W.BY_NAME[args.workload]
     oracle.build()
     n = os.cpu_count() or 1
-    per_worker = 4
+    per_worker = 8
     with mp.get_context("spawn").Pool(n, initializer=_ref_init, initargs=(w.name, n, per_worker)) as pool:
         for _ in range(args.warmup):
             pool.map(_ref_step, range(n), chunksize=1)
