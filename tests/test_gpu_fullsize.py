@@ -177,6 +177,30 @@ def test_fullsize_mixed_levels_streamed(orc):
     streamed = time.perf_counter() - t0
     assert cg.cg_read_status(ws) == cg.CG_OK
     assert T.equal(out, one_shot)
+    # the parts alone: the container's host-to-device copy, and the one-shot
+    # decode from device memory
+    T.cuda.synchronize()
+    t0 = time.perf_counter()
+    dev.copy_(cont_host, non_blocking=True)
+    T.cuda.synchronize()
+    t_copy = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    cg.check(cg.cg_decode(run.cfg, run.tables, dev, n, 0, -1, out, ws), "decode")
+    T.cuda.synchronize()
+    t_dec = time.perf_counter() - t0
+    # one cg_decode reading the container straight from pinned host memory
+    out.zero_()
+    T.cuda.synchronize()
+    t0 = time.perf_counter()
+    cg.check(cg.cg_decode(run.cfg, run.tables, cg.cg_host_mapped(cont_host), n, 0, -1, out, ws), "host decode")
+    T.cuda.synchronize()
+    direct = time.perf_counter() - t0
+    assert cg.cg_read_status(ws) == cg.CG_OK
+    assert T.equal(out, one_shot)
     print(f"\nstreamed decode of {w.n_chunks} chunks in groups of {group}: {streamed * 1e3:.1f} ms "
-          f"({w.fp16_bytes / streamed / 1e9:.0f} GB/s of fp16, {n / streamed / 1e9:.1f} GB/s of container)")
+          f"({w.fp16_bytes / streamed / 1e9:.0f} GB/s of fp16, {n / streamed / 1e9:.1f} GB/s of container); "
+          f"alone: copy {t_copy * 1e3:.1f} ms, decode {t_dec * 1e3:.1f} ms; overlap efficiency "
+          f"max(copy, decode) / streamed = {max(t_copy, t_dec) / streamed:.2f}; "
+          f"one decode from the pinned host container: {direct * 1e3:.1f} ms "
+          f"({w.fp16_bytes / direct / 1e9:.0f} GB/s of fp16)")
     _check_heads(orc, run, ch, levels, out)
