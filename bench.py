@@ -236,16 +236,16 @@ def workload_config(w, world):
 _REF = None  # a reference-arm worker's prepared streams
 
 
-def _ref_init(name, nworkers, per_worker):
-    """Reference-arm worker: generate, fit and encode (untimed) the chunk-0
-    streams of its heads, spread over the layers."""
+def _ref_init(name, nworkers, per_worker, ids):
+    """Reference-arm worker: take an index from ids, then generate, fit and
+    encode (untimed) the chunk-0 streams of its heads, spread over the
+    layers."""
     global _REF
-    import multiprocessing as mp
     sys.path.insert(0, ROOT)
     import oracle
     from kv_cache_compression_02_gb300 import synth, workloads as W
     w = W.BY_NAME[name]
-    widx = (mp.current_process()._identity or (1,))[0] - 1
+    widx = ids.get()
     nsi = w.L * 2 * w.H
     stride = max(1, nsi // (nworkers * per_worker))
     cd = oracle.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
@@ -284,7 +284,11 @@ def run_reference(args):
     oracle.build()
     n = os.cpu_count() or 1
     per_worker = 8
-    with mp.get_context("spawn").Pool(n, initializer=_ref_init, initargs=(w.name, n, per_worker)) as pool:
+    ctx = mp.get_context("spawn")
+    ids = ctx.Queue()
+    for i in range(n):
+        ids.put(i)
+    with ctx.Pool(n, initializer=_ref_init, initargs=(w.name, n, per_worker, ids)) as pool:
         for _ in range(args.warmup):
             pool.map(_ref_step, range(n), chunksize=1)
         nbytes = 0
