@@ -8,13 +8,16 @@ closed-loop deltas, rANS streams, size scan, compaction) and cg_decode
 resident in HBM when the timed region starts and are larger than L2.
 
 The headline value is decode throughput (fp16 GB/s written by cg_decode);
-encode and fit throughput, the compression ratio, the entropy bound of the
-coded symbols, roofline fractions, an end-to-end figure through host
+encode and fit throughput, the compression ratio (with and without the
+tables), roofline fractions, an end-to-end figure through host
 buffers, the same decode in layer groups (time to the first group) and into
 a paged (block-table) cache, and a bandwidth-adaptive streaming run (chunk
 levels chosen by the host controller over a simulated link, the planned
-container encoded and decoded on the GPU) are reported beside it.  `--impl reference` times the CPU oracle on
-a bounded sample of the same workload instead.
+container encoded and decoded on the GPU) are reported beside it.  (The
+container's size against the entropy bound of its coded symbols is a gate of
+the oracle tests, which reproduce the bytes exactly.)  `--impl reference`
+times the CPU oracle on every host core, on a bounded sample of the same
+workload, instead.
 
 Multi-GPU: every rank codes its own copy of the workload (independent
 problems, no collective on the data path); value = all ranks' bytes / the
