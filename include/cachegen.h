@@ -228,19 +228,22 @@ cg_status cg_decode_paged(const cg_dims *dims, const cg_params *params, const vo
                           void *stream);
 
 /* cg_decode without a workspace argument, for callers that cannot
- * allocate device memory: code running while a CUDA graph is captured,
- * allocator-free embedded runtimes, or a serving loop whose device memory
- * is all owned by its own pool.  (No counterpart in the CacheGen pages; it
- * is a deployment convenience.)  Arguments and results are those of
- * cg_decode; the decode workspace instead lives in a 64 KiB device array
- * inside the library, held by every GPU that loads it until exit, which
- * limits the container to 2040 chunks (CG_ERR_CAPACITY beyond).
+ * allocate device memory: allocator-free embedded runtimes, or a serving
+ * loop whose device memory is all owned by its own pool and may not grow.
+ * (No counterpart in the CacheGen pages; it is a deployment convenience.)
+ * Arguments and results are those of cg_decode (the same argument checks);
+ * the decode workspace instead lives in a 64 KiB device array inside the
+ * library, held by every GPU that loads it until exit, which limits the
+ * container to 2040 chunks (CG_ERR_CAPACITY beyond).
  *   status_ws: if not NULL, receives the device address of that array;
  *              pass it to cg_read_status() after synchronising.
- * The first call on each device looks the array's address up (make it
- * before any stream capture).  All calls share the array and it keeps the
- * last call's contents: each call clears the status first, and calls that
- * overlap on the GPU race on it, so serialise them.  It allocates nothing. */
+ * The first call on each device looks the array's address up and keeps it
+ * for the life of the process (make that first call before any stream
+ * capture); after cudaDeviceReset the kept address is stale, so do not call
+ * this entry point again in that process.  All calls share the array and it
+ * keeps the last call's contents: each call clears the status first, and
+ * calls that overlap on the GPU race on it, so serialise them.  It calls no
+ * allocating routine. */
 cg_status cg_decode_noalloc(const cg_dims *dims, const cg_params *params, const void *tables_dev,
                             const void *bitstream_dev, uint64_t bitstream_bytes,
                             int32_t chunk_begin, int32_t chunk_end, void *kv_dev, void *stream,

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libcachegen.so")
 SOURCES = ["cg_api.cu", "cg_fit.cu", "cg_encode.cu", "cg_decode.cu", "cg_noalloc.cu", "cg_plan.cu", "cg_assemble.cu"]
-HEADERS = ["cg_layout.cuh", "cg_kernels.cuh"]
+HEADERS = ["cg_layout.cuh", "cg_kernels.cuh", "cg_args.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

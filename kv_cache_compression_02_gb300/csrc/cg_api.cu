@@ -8,23 +8,12 @@
 #include <vector>
 
 #include "cachegen.h"
+#include "cg_args.h"
 #include "cg_kernels.cuh"
 
 using namespace cg;
 
 namespace {
-
-bool layout_of(const cg_dims *dm, const cg_params *pr, Layout &lo) {
-  if (!dm || !pr || dm->reserved != 0) return false;
-  if (!make_layout(lo, dm->L, dm->H, dm->d, dm->C, dm->G, dm->S, pr->alphabet_radius, pr->n_levels))
-    return false;
-  for (int i = 0; i < pr->n_levels; i++)
-    if (!std::isfinite(pr->level_base[i]) || !(pr->level_base[i] > 0.0f)) return false;
-  if (pr->layer_mult)
-    for (int i = 0; i < 2 * dm->L; i++)
-      if (!std::isfinite(pr->layer_mult[i]) || !(pr->layer_mult[i] > 0.0f)) return false;
-  return true;
-}
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 

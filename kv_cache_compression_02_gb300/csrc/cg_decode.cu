@@ -26,6 +26,8 @@
 // sets the CORRUPT bit.  Nothing waits on another CTA.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "cg_kernels.cuh"
 
 namespace cg {
@@ -126,6 +128,117 @@ __device__ __forceinline__ uint16_t *paged_row(const PagedOut &po, uint16_t *poo
   return pool + ((uint64_t(ok ? b : 0) * lo.H + h) * po.bt + tib) * lo.d + kLpt * i;
 }
 
+// ---------------------------------------------------------------- tables
+// A head's d frequency tables in shared memory, laid out so that thread i
+// of a team of T threads (lanes 4i..4i+3) only ever touches bank i: u16
+// position p of a table row holds the channel 4 ti + j with
+// p = (j >> 1) * 2T + 2 ti + (j & 1).
+template <int T>
+__device__ __forceinline__ int chan_of(int p) {
+  const int r = p % (2 * T);
+  return 4 * (r >> 1) + 2 * (p / (2 * T)) + (r & 1);
+}
+
+// The d cdf columns (global, [d][256] u16) -> cdfc rows 0..255, row 256
+// repeating cdf_255 (so that f_255, the escape, reads as 0) and a zero row
+// 257.  A thread takes 8 rows of one position (one 16-byte load);
+// neighbouring threads store neighbouring positions of a row.  A column
+// that does not start at 0 or does not strictly increase sets *bad.
+template <int T>
+__device__ __forceinline__ void build_cdf_columns(const uint16_t *cdf, uint16_t *cdfc, int *bad) {
+  constexpr int kRow = kLpt * T;
+  for (int e = threadIdx.x; e < 32 * kRow; e += blockDim.x) {
+    const int p = e % kRow, s0 = 8 * (e / kRow);
+    const uint16_t *src = cdf + chan_of<T>(p) * 256 + s0;
+    const uint4 v = *reinterpret_cast<const uint4 *>(src);
+    const uint32_t nx = s0 + 8 < 256 ? uint32_t(src[8]) : kM;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    bool b = s0 == 0 && (w[0] & 0xFFFFu) != 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const uint32_t c0 = (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+      const uint32_t c1 = q < 7 ? (w[(q + 1) >> 1] >> (16 * ((q + 1) & 1))) & 0xFFFFu : nx;
+      b |= c1 <= c0;
+      cdfc[(s0 + q) * kRow + p] = uint16_t(c0);
+      if (s0 + q == 255) cdfc[256 * kRow + p] = uint16_t(c0);
+    }
+    if (b) *bad = 1;
+  }
+  for (int p = threadIdx.x; p < kRow; p += blockDim.x) cdfc[257 * kRow + p] = 0;
+}
+
+// First symbol of the neighbouring pair (sa, sa + 1) holding most of the
+// slots [slot0, slot0 + width) of column colp (row stride kRow), where s is
+// the symbol at slot0.
+template <int kRow>
+__device__ __forceinline__ uint32_t densest_pair(const uint16_t *colp, uint32_t s, uint32_t slot0,
+                                                 uint32_t width) {
+  uint32_t sa = s, t = s, beg = slot0, prev = 0, best = 0;
+  for (;;) {
+    const uint32_t nt = t < 255 ? uint32_t(colp[(t + 1) * kRow]) : kM;
+    const uint32_t cnt = min(nt, slot0 + width) - beg;  // in-bucket slots of t
+    if (t > s && prev + cnt > best) {
+      best = prev + cnt;
+      sa = t - 1;
+    }
+    if (t == 255 || nt >= slot0 + width) break;
+    prev = cnt;
+    beg = nt;
+    t++;
+  }
+  return sa;
+}
+
+// Full bucket entries: lut16 [512 buckets][row] u16 = sa << 8 | (255 - last
+// offset of sa in the 128-slot bucket).  A thread walks 64 buckets of the
+// two positions of one 32-bit word, carrying the current symbol from bucket
+// to bucket.
+template <int T>
+__device__ __forceinline__ void build_lut16(uint16_t *lut16, const uint16_t *cdfc) {
+  constexpr int kRow = kLpt * T;
+  for (int e = threadIdx.x; e < 8 * 2 * T; e += blockDim.x) {
+    const int wd = e % (2 * T), b0 = 64 * (e / (2 * T));
+#pragma unroll
+    for (int hpos = 0; hpos < 2; hpos++) {
+      const uint16_t *colp = cdfc + 2 * wd + hpos;
+      uint32_t s = 0;  // largest s with cdf_s <= 128 b0 (cdf_0 = 0)
+#pragma unroll
+      for (uint32_t stp = 128; stp; stp >>= 1)
+        if (s + stp <= 255 && colp[(s + stp) * kRow] <= kBucketSlots * b0) s += stp;
+      for (int bb = 0; bb < 64; bb++) {
+        const uint32_t slot0 = kBucketSlots * (b0 + bb);
+        while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
+        const uint32_t sa = densest_pair<kRow>(colp, s, slot0, kBucketSlots);
+        const uint32_t nxt = sa < 255 ? uint32_t(colp[(sa + 1) * kRow]) : kM;
+        const uint32_t bnd = min(nxt - slot0, kBucketSlots) - 1;  // last slot of sa in the bucket
+        lut16[(b0 + bb) * kRow + 2 * wd + hpos] = uint16_t((sa << 8) | (255 - bnd));
+      }
+    }
+  }
+}
+
+// Compact bucket entries: lut8 [256 buckets][4 lanes x T] u8 = sa of each
+// 256-slot bucket (at most 254), thread i's four lanes in word i.
+template <int T>
+__device__ __forceinline__ void build_lut8(uint8_t *lut8, const uint16_t *cdfc) {
+  constexpr int kRow = kLpt * T;
+  for (int e = threadIdx.x; e < 4 * kRow; e += blockDim.x) {
+    const int c = e % kRow, b0 = 64 * (e / kRow);
+    const int ti = c >> 2, j = c & 3;
+    const uint16_t *colp = cdfc + (j >> 1) * 2 * T + 2 * ti + (j & 1);
+    uint32_t s = 0;
+#pragma unroll
+    for (uint32_t stp = 128; stp; stp >>= 1)
+      if (s + stp <= 255 && colp[(s + stp) * kRow] <= kCBucketSlots * b0) s += stp;
+    for (int bb = 0; bb < 64; bb++) {
+      const uint32_t slot0 = kCBucketSlots * (b0 + bb);
+      while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
+      const uint32_t sa = densest_pair<kRow>(colp, s, slot0, kCBucketSlots);
+      lut8[(b0 + bb) * kRow + c] = uint8_t(min(sa, 254u));
+    }
+  }
+}
+
 // ---------------------------------------------------------------- decode
 // Shared memory per CTA (d lanes, T = d/4 threads per team), 215 KB at d=128
 // with 22 teams:
@@ -177,103 +290,10 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
                         tab_index(lo, lv, l, kvi, h * lo.d) * 256;
   constexpr int kRow = kLpt * T;  // u16 entries per table row
-  // u16 position p of a row holds the channel 4 * ti + j with
-  // p = (j >> 1) * 2T + 2 ti + (j & 1)
-  auto chan_of = [](int p) { const int r = p % (2 * T); return 4 * (r >> 1) + 2 * (p / (2 * T)) + (r & 1); };
-  // cdf columns: a thread takes 8 rows of one position (one 16-byte load);
-  // neighbouring threads store neighbouring positions of a row
-  for (int e = threadIdx.x; e < 32 * kRow; e += blockDim.x) {
-    const int p = e % kRow, s0 = 8 * (e / kRow);
-    const uint16_t *src = cdf + chan_of(p) * 256 + s0;
-    const uint4 v = *reinterpret_cast<const uint4 *>(src);
-    const uint32_t nx = s0 + 8 < 256 ? uint32_t(src[8]) : kM;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    bool bad = s0 == 0 && (w[0] & 0xFFFFu) != 0;
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      const uint32_t c0 = (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-      const uint32_t c1 = q < 7 ? (w[(q + 1) >> 1] >> (16 * ((q + 1) & 1))) & 0xFFFFu : nx;
-      bad |= c1 <= c0;
-      cdfc[(s0 + q) * kRow + p] = uint16_t(c0);
-      if (s0 + q == 255) cdfc[256 * kRow + p] = uint16_t(c0);  // row 256 = cdf_255: f_255 reads as 0
-    }
-    if (bad) s_bad = 1;
-  }
-  for (int p = threadIdx.x; p < kRow; p += blockDim.x) cdfc[257 * kRow + p] = 0;  // pad row
+  build_cdf_columns<T>(cdf, cdfc, &s_bad);
   __syncthreads();
-  // bucket entries: a thread walks 64 buckets of the two positions of one
-  // 32-bit word, carrying the current symbol from bucket to bucket
-  if constexpr (COMPACT) {
-    // one lane's 64 buckets per thread: sa of each 256-slot bucket
-    for (int e = threadIdx.x; e < 4 * kRow; e += blockDim.x) {
-      const int c = e % kRow, b0 = 64 * (e / kRow);
-      const int ti = c >> 2, j = c & 3;
-      const uint16_t *colp = cdfc + (j >> 1) * 2 * T + 2 * ti + (j & 1);
-      uint32_t s = 0;
-#pragma unroll
-      for (uint32_t stp = 128; stp; stp >>= 1)
-        if (s + stp <= 255 && colp[(s + stp) * kRow] <= kCBucketSlots * b0) s += stp;
-      for (int bb = 0; bb < 64; bb++) {
-        const uint32_t slot0 = kCBucketSlots * (b0 + bb);
-        while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
-        uint32_t sa = s;
-        {
-          uint32_t t = s, beg = slot0, prev = 0, best = 0;
-          for (;;) {
-            const uint32_t nt = t < 255 ? uint32_t(colp[(t + 1) * kRow]) : kM;
-            const uint32_t cnt = min(nt, slot0 + kCBucketSlots) - beg;
-            if (t > s && prev + cnt > best) {
-              best = prev + cnt;
-              sa = t - 1;
-            }
-            if (t == 255 || nt >= slot0 + kCBucketSlots) break;
-            prev = cnt;
-            beg = nt;
-            t++;
-          }
-        }
-        lut8[(b0 + bb) * kRow + c] = uint8_t(min(sa, 254u));
-      }
-    }
-  } else
-  for (int e = threadIdx.x; e < 8 * 2 * T; e += blockDim.x) {
-    const int wd = e % (2 * T), b0 = 64 * (e / (2 * T));
-#pragma unroll
-    for (int hpos = 0; hpos < 2; hpos++) {
-      const uint16_t *colp = cdfc + 2 * wd + hpos;
-      // largest s with cdf_s <= 128 b0 (cdf_0 = 0)
-      uint32_t s = 0;
-#pragma unroll
-      for (uint32_t stp = 128; stp; stp >>= 1)
-        if (s + stp <= 255 && colp[(s + stp) * kRow] <= kBucketSlots * b0) s += stp;
-      for (int bb = 0; bb < 64; bb++) {
-        const uint32_t slot0 = kBucketSlots * (b0 + bb);
-        while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
-        // the neighbouring pair (sa, sa + 1) holding most slots of the bucket
-        uint32_t sa = s;
-        {
-          uint32_t t = s, beg = slot0, prev = 0, best = 0;
-          for (;;) {
-            const uint32_t nt = t < 255 ? uint32_t(colp[(t + 1) * kRow]) : kM;
-            const uint32_t cnt = min(nt, slot0 + kBucketSlots) - beg;  // in-bucket slots of t
-            if (t > s && prev + cnt > best) {
-              best = prev + cnt;
-              sa = t - 1;
-            }
-            if (t == 255 || nt >= slot0 + kBucketSlots) break;
-            prev = cnt;
-            beg = nt;
-            t++;
-          }
-        }
-        const uint32_t nxt = sa < 255 ? uint32_t(colp[(sa + 1) * kRow]) : kM;
-        const uint32_t bnd = min(nxt - slot0, kBucketSlots) - 1;  // last slot of sa in the bucket
-        const uint32_t v = (sa << 8) | (255 - bnd);
-        if (hpos == 0) lut16[(b0 + bb) * kRow + 2 * wd] = uint16_t(v);
-        else lut16[(b0 + bb) * kRow + 2 * wd + 1] = uint16_t(v);
-      }
-    }
-  }
+  if constexpr (COMPACT) build_lut8<T>(lut8, cdfc);
+  else build_lut16<T>(lut16, cdfc);
   __syncthreads();
   if (s_bad) {
     if (threadIdx.x == 0) atomicOr(status, kStCorrupt);
@@ -657,6 +677,371 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   }
 }
 
+// ---------------------------------------------------------------- d = 128
+// The decoder for d = 128 (the models' head dim).  One CTA per (level,
+// head), a warp per chunk stream, thread i on lanes 4i..4i+3, as k_decode,
+// with tables laid out for a short token loop:
+//   - main  [256 buckets][128] u16: for the 256-slot bucket slot >> 8, the
+//           first symbol sa of the neighbouring pair holding most of it and
+//           the last offset of sa's range in it (sa << 8 | 255 - offset),
+//           so one carry out of the low byte picks sa or sa + 1;
+//   - fine  [256][128] u16, the same entries for 16-slot buckets over the
+//           two ends of the slot range, [0, 2048) and [63488, 65536): the
+//           distribution tails, where a 256-slot bucket holds many narrow
+//           symbols;
+//   - cdfc  [258][128] u16 as k_decode's (row 256 repeats cdf_255).
+// Each table row holds the 128 channels with thread i's lanes at byte 4i
+// of each 128-byte half (bank i), addressed by 32-bit byte offsets.  For a
+// lane with state x the main entry's row is x & 0xFF00; a main entry of a
+// tail bucket is 0xFFFF, and the lane takes the fine entry at row
+// (x << 4) & 0xFF00 instead (bits 4..11 of the slot: rows 0..127 for the low
+// end, 128..255 for the high end).  The carry out of (x & 255) + entry gives
+// t with t & 0xFF00 = symbol * 256: the symbol's cdf row offset and, OR-ed
+// into the bits of 2^15, the exact fp32 2^15 + symbol.  A lane whose slot
+// still falls outside the pair (about 0.1% on the 70B-shaped workload), or
+// whose symbol is the escape, is resolved by a binary search of its cdf
+// column; one warp vote per token guards that path.  Words are staged per warp in a
+// ring of two halves: the token that crosses into the second half waits for
+// it and, after its reads, refills the consumed half.
+constexpr uint32_t kMainOff = 0;                        // main [256][128] u16
+constexpr uint32_t kFineOff = 256 * 256;                // fine [256][128] u16
+constexpr uint32_t kCdfOff = 2 * 256 * 256;             // cdfc [258][128] u16
+constexpr uint32_t kRingOff = kCdfOff + kCdfRows * 256; // rings [teams][kRing + kMirror] u16
+constexpr uint32_t kRingStride = kRing + kMirror;       // words per warp ring
+constexpr uint32_t kTail = 2048;                        // slots covered by the fine table at each end
+constexpr int kTeams128Max = 24;
+
+// byte offset of lane j of thread 0 in a table row (thread i adds 4 i)
+template <int J>
+__device__ __forceinline__ constexpr uint32_t colb() { return (J >> 1) * 128 + (J & 1) * 2; }
+
+__device__ __forceinline__ uint32_t lds16(const uint8_t *sm, uint32_t off) {
+  return *reinterpret_cast<const uint16_t *>(sm + off);
+}
+
+// Inclusive warp scan step: v += (value of lane i - O, when there is one).
+template <int O>
+__device__ __forceinline__ uint32_t scan_step(uint32_t v) {
+  asm("{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+      "shfl.sync.up.b32 t|p, %0, %1, 0, -1;\n\t"
+      "@p add.u32 %0, %0, t;\n\t}"
+      : "+r"(v) : "n"(O));
+  return v;
+}
+
+// Pair entries for nb consecutive buckets of `width` slots (a power of two
+// up to 256) from slot `base`: entry b of column c is sa << 8 | (255 - the
+// last offset of sa's range in the bucket - bias), where (sa, sa + 1) is the
+// neighbouring pair holding most of the bucket.  For 16-slot buckets bias is
+// the bucket's offset in its 256-slot bucket (16 (b mod 16)), so that the
+// carry out of (x & 255) + entry is the same test as for the main table.
+// Buckets below flag_lo or from flag_hi get 0xFFFF instead.  A thread walks
+// 32 buckets of the two positions of one 32-bit word of the row, carrying
+// the current symbol from bucket to bucket.
+__device__ __forceinline__ void build_pairs(uint16_t *lut, const uint16_t *cdfc, int nb, uint32_t width,
+                                            uint32_t base, int flag_lo, int flag_hi) {
+  constexpr int kRowU = 128, kRun = 32;
+  for (int e = threadIdx.x; e < (nb / kRun) * 64; e += blockDim.x) {
+    const int wd = e % 64, b0 = kRun * (e / 64);
+#pragma unroll
+    for (int hpos = 0; hpos < 2; hpos++) {
+      const uint16_t *colp = cdfc + 2 * wd + hpos;
+      uint32_t s = 0;  // largest s with cdf_s <= the run's first slot (cdf_0 = 0)
+#pragma unroll
+      for (uint32_t stp = 128; stp; stp >>= 1)
+        if (s + stp <= 255 && colp[(s + stp) * kRowU] <= base + width * b0) s += stp;
+      for (int bb = 0; bb < kRun; bb++) {
+        const int b = b0 + bb;
+        const uint32_t slot0 = base + width * b;
+        while (s < 255 && colp[(s + 1) * kRowU] <= slot0) s++;
+        uint16_t v = 0xFFFFu;
+        if (b >= flag_lo && b < flag_hi) {
+          const uint32_t sa = densest_pair<kRowU>(colp, s, slot0, width);
+          const uint32_t nxt = sa < 255 ? uint32_t(colp[(sa + 1) * kRowU]) : kM;
+          const uint32_t bnd = min(nxt - slot0, width) - 1;  // last offset of sa in the bucket
+          const uint32_t bias = width < 256 ? width * (uint32_t(b) & (256 / width - 1)) : 0u;
+          v = uint16_t((sa << 8) | (255 - bnd - bias));
+        }
+        lut[b * kRowU + 2 * wd + hpos] = v;
+      }
+    }
+  }
+}
+
+// Slow lane J (a slot outside the pair its bucket entry names, or the
+// escape symbol, whose frequency reads as 0): a binary search of the lane's
+// cdf column.  Replaces the lane's frequency, offset in range and symbol
+// row (symbol << 8); marks an escape in escm.
+template <int J>
+__device__ __forceinline__ void slow128(const uint8_t *sm, uint32_t i4, uint32_t x, uint32_t &ff, uint32_t &rr,
+                                        uint32_t &ro, uint32_t &escm) {
+  const uint32_t col = i4 + colb<J>();
+  const uint32_t slot = x & 0xFFFFu;
+  uint32_t s = 0;  // largest s with cdf_s <= slot (cdf_0 = 0)
+#pragma unroll
+  for (uint32_t stp = 128; stp; stp >>= 1)
+    if (lds16(sm, kCdfOff + ((s + stp) << 8) + col) <= slot) s += stp;
+  const uint32_t c0 = lds16(sm, kCdfOff + (s << 8) + col);
+  const uint32_t c1 = s < 255 ? lds16(sm, kCdfOff + ((s + 1) << 8) + col) : kM;
+  ff = c1 - c0;
+  rr = slot - c0;
+  ro = s << 8;
+  if (s == uint32_t(kEsc)) escm |= 1u << J;
+}
+
+template <bool PAGED>
+__global__ void __launch_bounds__(kTeams128Max * 32, 1)
+k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
+         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
+  constexpr int T = 32;
+  extern __shared__ __align__(16) uint8_t smb[];
+  __shared__ int s_bad;
+  uint16_t *cdfc = reinterpret_cast<uint16_t *>(smb + kCdfOff);
+
+  const int lv = blockIdx.x, si = blockIdx.y;
+  if (si < si_lo || si >= si_hi) return;  // outside the requested layers
+  const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
+  if (cnt == 0) return;
+  const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
+  uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+  const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
+                        tab_index(lo, lv, l, kvi, h * lo.d) * 256;
+  build_cdf_columns<T>(cdf, cdfc, &s_bad);
+  __syncthreads();
+  // main entries of the tail buckets (the first and last 8) point to the fine table
+  build_pairs(reinterpret_cast<uint16_t *>(smb + kMainOff), cdfc, 256, 256, 0, kTail / 256, 256 - kTail / 256);
+  build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff), cdfc, 128, 16, 0, 0, 128);
+  build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff) + 128 * 128, cdfc, 128, 16, kM - kTail, 0, 128);
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) atomicOr(status, kStCorrupt);
+    return;
+  }
+
+  const int team = threadIdx.x >> 5, nteams = blockDim.x >> 5;
+  const uint32_t i = threadIdx.x & 31, i4 = 4 * i;
+  const float4 st4 = *reinterpret_cast<const float4 *>(
+      reinterpret_cast<const float *>(tables + lo.tb_step) + tab_index(lo, lv, l, kvi, h * lo.d + i4));
+  const float step[4] = {st4.x, st4.y, st4.z, st4.w};
+  uint16_t *ring = reinterpret_cast<uint16_t *>(smb + kRingOff) + team * kRingStride;
+
+  for (int idx = team; idx < cnt; idx += nteams) {
+    const int k = list[idx];
+    const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k), nd = chunk_nd(lo, k);
+    const uint64_t base = ld_u64(buf + 64 + 8 * uint64_t(k));
+    const uint64_t cend = (k + 1 < lo.n_chunks) ? ld_u64(buf + 64 + 8 * uint64_t(k + 1)) : ld_u64(buf + 48);
+    const uint8_t *chunk = buf + base;
+    const uint32_t *soffv = reinterpret_cast<const uint32_t *>(chunk + chunk_sec_off(lo, k));
+    const uint64_t so = soffv[si];
+    const uint64_t se = (si + 1 < lo.nstr) ? uint64_t(soffv[si + 1]) : (cend - base);
+    bool ok = !(so & 15) && so >= chunk_fixed(lo, k) && se >= so && base + se <= cend &&
+              se - so >= 16 + 4 * uint64_t(lo.d);
+    const uint8_t *blk = chunk + so;
+    uint32_t nw = 0, ne = 0;
+    if (ok) {
+      const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+      nw = hdr.x;
+      ne = hdr.y;
+      ok = hdr.z == uint32_t(nd) && hdr.w == 0 && 16 + 4 * uint64_t(lo.d) + 2 * uint64_t(nw) <= se - so;
+    }
+    if (!ok) {
+      if (i == 0) atomicOr(status, kStCorrupt);
+      continue;
+    }
+    const uint4 xs = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * i);
+    uint32_t x[4] = {xs.x, xs.y, xs.z, xs.w};
+    const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
+    const uint32_t wbytes = 2 * nw;
+    auto load_half = [&](uint32_t w0) {  // words [w0, w0 + kHalf) -> ring half, zero past the end
+      for (uint32_t o = 16 * i; o < 2 * kHalf; o += 16 * T) {
+        const uint32_t b = 2 * w0 + o;
+        const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
+        cp_async16(ring + ((w0 + o / 2) & (kRing - 1)), reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
+      }
+      if ((w0 & (kRing - 1)) == 0 && 16 * i < 2 * kMirror) {  // the mirror of ring[0, kMirror)
+        const uint32_t b = 2 * w0 + 16 * i;
+        const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
+        cp_async16(ring + kRing + 8 * i, reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
+      }
+      cp_async_commit();
+    };
+    __syncwarp();  // the previous stream's reads of this ring are done
+    load_half(0);
+    load_half(kHalf);
+    // the ring holds words [rbase, rbase + kRing); words below lim (<= nw)
+    // are known to have landed
+    uint32_t rbase = 0, lim = 0, p = 0, nesc = 0;
+    const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + i4) * 4);
+    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + i4;
+    bool broken = false;
+
+    // output row of the current token
+    uint16_t *orow;
+    bool row_ok = true, bad_row = false;
+    [[maybe_unused]] uint16_t *pool = nullptr;
+    [[maybe_unused]] int64_t lblk = 0, lblk_end = 0;
+    [[maybe_unused]] int left = 0;
+    [[maybe_unused]] int32_t bnext = 0;
+    if constexpr (PAGED) {
+      pool = po.pools[l * 2 + kvi];
+      const int64_t t0 = int64_t(k) * lo.C;
+      lblk = t0 / po.bt;
+      lblk_end = (t0 + ntok - 1) / po.bt + 1;
+      const int tib = int(t0 - lblk * po.bt);
+      left = po.bt - tib;
+      orow = paged_row(po, pool, po.table[lblk], tib, h, lo, int(i), row_ok);
+      bad_row = !row_ok;
+      if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
+    } else {
+      orow = kv + (uint64_t(si) * lo.S + uint64_t(k) * lo.C) * lo.d + i4;
+    }
+    auto next_row = [&]() {
+      if constexpr (PAGED) {
+        if (--left == 0) {
+          left = po.bt;
+          if (++lblk < lblk_end) {
+            orow = paged_row(po, pool, bnext, 0, h, lo, int(i), row_ok);
+            bad_row |= !row_ok;
+            if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
+          }
+        } else {
+          orow += lo.d;
+        }
+      } else {
+        orow += lo.d;
+      }
+    };
+    auto store_row = [&](float v0, float v1, float v2, float v3) {
+      if (!PAGED || row_ok) *reinterpret_cast<uint2 *>(orow) = make_uint2(pack_f16x2(v0, v1), pack_f16x2(v2, v3));
+    };
+
+    uint32_t a4n = *reinterpret_cast<const uint32_t *>(anc);  // next group's anchors, loaded ahead
+    for (int g = 0; g < ng && !broken; g++) {
+      const uint32_t a4 = a4n;
+      if (g + 1 < ng) a4n = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g + 1) * lo.d);
+      float ah[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
+      store_row(ah[0], ah[1], ah[2], ah[3]);
+      next_row();
+      const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
+      for (int tt = 0; tt < nt; tt++) {
+        // ---- symbol search in the main table
+        uint32_t ff[4], rr[4], ro[4];
+        bool sl[4];
+#define CG_LOOKUP(J)                                                                   \
+  {                                                                                    \
+    const uint32_t xx = x[J];                                                          \
+    uint32_t lu = lds16(smb, kMainOff + colb<J>() + ((xx & 0xFF00u) | i4));            \
+    if (lu >= 0xFF00u) lu = lds16(smb, kFineOff + colb<J>() + (((xx << 4) & 0xFF00u) | i4)); \
+    const uint32_t t = (xx & 0xFFu) + lu;                                              \
+    const uint32_t r = (t & 0xFF00u) | i4;                                    \
+    const uint32_t c0 = lds16(smb, kCdfOff + colb<J>() + r);                  \
+    const uint32_t c1 = lds16(smb, kCdfOff + 256 + colb<J>() + r);            \
+    ff[J] = c1 - c0;                                                          \
+    rr[J] = (xx - c0) & 0xFFFFu;                                              \
+    ro[J] = t & 0xFF00u;                                                      \
+    sl[J] = rr[J] >= ff[J];                                                   \
+  }
+        CG_LOOKUP(0)
+        CG_LOOKUP(1)
+        CG_LOOKUP(2)
+        CG_LOOKUP(3)
+#undef CG_LOOKUP
+        uint32_t escm = 0, cntw = 0;
+        bool esc_warp = false;
+        if (__any_sync(0xffffffffu, sl[0] | sl[1] | sl[2] | sl[3])) {
+          if (sl[0]) slow128<0>(smb, i4, x[0], ff[0], rr[0], ro[0], escm);
+          if (sl[1]) slow128<1>(smb, i4, x[1], ff[1], rr[1], ro[1], escm);
+          if (sl[2]) slow128<2>(smb, i4, x[2], ff[2], rr[2], ro[2], escm);
+          if (sl[3]) slow128<3>(smb, i4, x[3], ff[3], rr[3], ro[3], escm);
+          cntw = 2 * __popc(escm);  // an escape's raw value takes two words
+          esc_warp = __any_sync(0xffffffffu, escm != 0);
+        }
+        // ---- state update, word counts, word positions
+        bool ndf[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          x[j] = ff[j] * (x[j] >> 16) + rr[j];
+          ndf[j] = x[j] < kRansL;
+          cntw += ndf[j] ? 1u : 0u;
+        }
+        uint32_t incl = scan_step<1>(cntw);
+        incl = scan_step<2>(incl);
+        incl = scan_step<4>(incl);
+        incl = scan_step<8>(incl);
+        incl = scan_step<16>(incl);
+        const uint32_t pn = p + __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t pos = p + incl - cntw;
+        if (pn > lim) {  // words past those known to have landed (or past the stream's end)
+          if (pn > nw) {
+            broken = true;
+            break;
+          }
+          cp_async_wait_all();
+          __syncwarp();
+          lim = min(nw, rbase + kRing);
+        }
+        float v[4];
+        if (!esc_warp) {
+          // ---- the thread's words are consecutive from pos: read four (the
+          // mirror covers reads past the ring's end; unneeded ones are
+          // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
+          const uint16_t *rp = ring + (pos & (kRing - 1));
+          const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3];
+          const uint32_t a1 = ndf[0] ? w1 : w0, a2 = ndf[0] ? w2 : w1, a3 = ndf[0] ? w3 : w2;
+          const uint32_t b2 = ndf[1] ? a2 : a1, b3 = ndf[1] ? a3 : a2;
+          const uint32_t wl[4] = {w0, a1, b2, ndf[2] ? b3 : b2};
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if (ndf[j]) x[j] = __byte_perm(wl[j], x[j], 0x5410);  // x<<16 | w
+            // q = symbol - 127 exactly: (2^15 + symbol) - (2^15 + 127)
+            v[j] = __fmaf_rn(__int_as_float(ro[j] | 0x47000000u) - 32895.0f, step[j], ah[j]);
+          }
+        } else {
+          // ---- escapes: the raw q follows the lane's renormalisation word;
+          // read the words from the container itself
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            if (ndf[j]) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
+            if ((escm >> j) & 1u) {
+              const int q = int(uint32_t(words[pos]) | (uint32_t(words[pos + 1]) << 16));
+              pos += 2;
+              nesc++;
+              v[j] = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
+            } else {
+              v[j] = __fmaf_rn(__int_as_float(ro[j] | 0x47000000u) - 32895.0f, step[j], ah[j]);
+            }
+          }
+        }
+        p = pn;
+        if (pn > rbase + kHalf) {  // the first half is consumed: refill it with the next words
+          __syncwarp();            // every thread's reads of it are done
+          cp_async_wait_all();     // and the other half has landed before it becomes the first
+          do {
+            load_half(rbase + kRing);
+            rbase += kHalf;
+          } while (pn > rbase + kHalf);
+          lim = min(lim, rbase + kHalf);
+        }
+        store_row(v[0], v[1], v[2], v[3]);
+        next_row();
+      }
+    }
+    cp_async_wait_all();
+    if (PAGED && bad_row) atomicOr(status, kStBadArg);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) nesc += __shfl_xor_sync(0xffffffffu, nesc, o);
+    const bool lanes_ok = x[0] == kRansL && x[1] == kRansL && x[2] == kRansL && x[3] == kRansL;
+    if (broken || !lanes_ok || p != nw || nesc != ne) atomicOr(status, kStCorrupt);
+  }
+}
+
 template <int T, bool PAGED, bool COMPACT>
 cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
                               uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po, int l0, int l1) {
@@ -672,6 +1057,21 @@ cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uin
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
   k_decode<T, PAGED, COMPACT>
       <<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  return cudaGetLastError();
+}
+
+// d = 128, full tables: k_dec128 with a warp per chunk of the CTA's level
+// (at least 16 warps, so that the table build is spread wide; warps without
+// a chunk only build).
+template <bool PAGED>
+cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
+                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+  const int teams = chunks > kTeams128Max ? kTeams128Max : (chunks < 16 ? 16 : chunks);
+  const size_t smem = kRingOff + size_t(teams) * kRingStride * 2;
+  cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
+  k_dec128<PAGED><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
 }
 
@@ -693,6 +1093,7 @@ cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint
     const int teams = chunks <= 12 ? (chunks < 8 ? 8 : chunks) : 12;
     return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
   }
+  if constexpr (T == 32) return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
   const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
   return launch_decode_tpb<T, PAGED, false>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
 }

@@ -1,13 +1,12 @@
 // cg_noalloc.cu -- cg_decode_noalloc: the decoder for callers that cannot
 // allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA
-// graph that is being captured, allocator-free embedded runtimes, or a
-// serving loop that has handed the whole device to its own memory pool and
-// may not grow it.  They own their inputs and outputs but cannot provide
-// the small decode workspace (status word and per-level chunk lists) that
-// cg_decode takes.  This entry point runs the same decode kernels with that
-// workspace in a file-scope device array instead.
+// Some callers cannot call cudaMalloc at all: allocator-free embedded
+// runtimes, or a serving loop that has handed the whole device to its own
+// memory pool and may not grow it.  They own their inputs and outputs but
+// cannot provide the small decode workspace (status word and per-level
+// chunk lists) that cg_decode takes.  This entry point runs the same decode
+// kernels with that workspace in a file-scope device array instead.
 //
 // The array is kNoallocScratchBytes (64 KiB) in every GPU that loads the
 // library, held until the process exits.  All calls share it and it keeps
@@ -15,10 +14,10 @@
 // calls that overlap on the GPU race on it.
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <mutex>
 
 #include "cachegen.h"
+#include "cg_args.h"
 #include "cg_kernels.cuh"
 
 namespace {
@@ -32,7 +31,9 @@ std::mutex g_mu;
 void *g_addr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device (host code only sees a stand-in symbol, not a device address).
+// device and kept for the life of the process (host code only sees a
+// stand-in symbol, not a device address; a cudaDeviceReset makes the kept
+// address stale).
 cudaError_t scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -49,15 +50,6 @@ cudaError_t scratch_address(void **out) {
   return cudaSuccess;
 }
 
-bool valid_config(const cg_dims *dm, const cg_params *pr, cg::Layout &lo) {
-  if (!dm || !pr || dm->reserved != 0) return false;
-  if (!cg::make_layout(lo, dm->L, dm->H, dm->d, dm->C, dm->G, dm->S, pr->alphabet_radius, pr->n_levels))
-    return false;
-  for (int i = 0; i < pr->n_levels; i++)
-    if (!std::isfinite(pr->level_base[i]) || !(pr->level_base[i] > 0.0f)) return false;
-  return true;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
@@ -68,7 +60,7 @@ extern "C" cg_status cg_decode_noalloc(const cg_dims *dims, const cg_params *par
                                        int32_t chunk_end, void *kv_dev, void *stream,
                                        const void **status_ws) {
   cg::Layout lo;
-  if (!valid_config(dims, params, lo) || !tables_dev || !bitstream_dev || !kv_dev)
+  if (!cg::layout_of(dims, params, lo) || !tables_dev || !bitstream_dev || !kv_dev)
     return CG_ERR_INVALID_ARG;
   if (!aligned16(tables_dev) || !aligned16(bitstream_dev) || !aligned16(kv_dev))
     return CG_ERR_INVALID_ARG;

@@ -106,3 +106,18 @@ def test_invalid_arguments(lib):
     assert lib.cg_assemble(*asm(ptrs, sizes, None)) == cg.CG_ERR_INVALID_ARG
     bad = (ctypes.c_uint8 * 1)(1)  # level 1 of a one-level configuration
     assert lib.cg_assemble(*asm(ptrs, sizes, bad)) == cg.CG_ERR_INVALID_ARG
+
+
+def test_decode_entry_points_validate_alike(lib):
+    """cg_decode and cg_decode_noalloc share their argument checks: a
+    non-finite or non-positive layer multiplier (or level base) is rejected by
+    both, synchronously and before any CUDA call."""
+    fake = 1 << 20  # an aligned non-null address that is never dereferenced
+    for mult in (float("nan"), float("inf"), 0.0, -1.0):
+        cfg = cg.Config(L=2, H=1, d=8, S=10, C=10, layer_mult=np.array([[1.0, 1.0], [mult, 1.0]], np.float32))
+        d, p = ctypes.byref(cfg.dims), ctypes.byref(cfg.params)
+        assert lib.cg_decode(d, p, fake, fake, 4096, 0, -1, fake, fake, 1 << 20, None) == cg.CG_ERR_INVALID_ARG
+        assert lib.cg_decode_noalloc(d, p, fake, fake, 4096, 0, -1, fake, None, None) == cg.CG_ERR_INVALID_ARG
+    cfg = cg.Config(L=1, H=1, d=8, S=10, C=10, level_base=(float("nan"),))
+    d, p = ctypes.byref(cfg.dims), ctypes.byref(cfg.params)
+    assert lib.cg_decode_noalloc(d, p, fake, fake, 4096, 0, -1, fake, None, None) == cg.CG_ERR_INVALID_ARG

@@ -1,5 +1,5 @@
 """cg_decode_noalloc: the decoder for callers that cannot allocate device
-memory (graph capture, allocator-free runtimes, a pool-owned device).
+memory (allocator-free runtimes, a device owned by the caller's own pool).
 
 It must decode exactly what cg_decode decodes, twice in a row through the
 same shared library scratch, and report its status through that scratch.
