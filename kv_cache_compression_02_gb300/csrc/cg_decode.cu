@@ -978,20 +978,11 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         incl = scan_step<16>(incl);
         const uint32_t pn = p + __shfl_sync(0xffffffffu, incl, 31);
         uint32_t pos = p + incl - cntw;
-        if (pn > lim) {  // words past those known to have landed (or past the stream's end)
-          if (pn > nw) {
-            broken = true;
-            break;
-          }
-          cp_async_wait_all();
-          __syncwarp();
-          lim = min(nw, rbase + kRing);
-        }
         float v[4];
-        if (!esc_warp) {
-          // ---- the thread's words are consecutive from pos: read four (the
-          // mirror covers reads past the ring's end; unneeded ones are
-          // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
+        // the thread's words are consecutive from pos: read four from the
+        // ring (the mirror covers reads past its end; unneeded ones are
+        // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
+        const auto ring_words = [&]() {
           const uint16_t *rp = ring + (pos & (kRing - 1));
           const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3];
           const uint32_t a1 = ndf[0] ? w1 : w0, a2 = ndf[0] ? w2 : w1, a3 = ndf[0] ? w3 : w2;
@@ -1003,32 +994,47 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
             // q = symbol - 127 exactly: (2^15 + symbol) - (2^15 + 127)
             v[j] = __fmaf_rn(__int_as_float(ro[j] | 0x47000000u) - 32895.0f, step[j], ah[j]);
           }
-        } else {
-          // ---- escapes: the raw q follows the lane's renormalisation word;
-          // read the words from the container itself
+        };
+        if (pn > lim || esc_warp) {  // (warp-uniform)
+          // ---- rare token: its words reach past those known to have
+          // landed (or past the stream's end), or an escape's raw value is
+          // among them
+          if (pn > nw) {
+            broken = true;
+            break;
+          }
+          cp_async_wait_all();  // every word issued so far has landed
+          __syncwarp();
+          if (!esc_warp) {
+            ring_words();
+          } else {
+            // escapes: the raw q follows the lane's renormalisation word;
+            // read the words from the container itself
 #pragma unroll
-          for (int j = 0; j < 4; j++) {
-            if (ndf[j]) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
-            if ((escm >> j) & 1u) {
-              const int q = int(uint32_t(words[pos]) | (uint32_t(words[pos + 1]) << 16));
-              pos += 2;
-              nesc++;
-              v[j] = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
-            } else {
-              v[j] = __fmaf_rn(__int_as_float(ro[j] | 0x47000000u) - 32895.0f, step[j], ah[j]);
+            for (int j = 0; j < 4; j++) {
+              if (ndf[j]) x[j] = __byte_perm(uint32_t(words[pos++]), x[j], 0x5410);
+              if ((escm >> j) & 1u) {
+                const int q = int(uint32_t(words[pos]) | (uint32_t(words[pos + 1]) << 16));
+                pos += 2;
+                nesc++;
+                v[j] = __fmaf_rn(__int2float_rn(q), step[j], ah[j]);
+              } else {
+                v[j] = __fmaf_rn(__int_as_float(ro[j] | 0x47000000u) - 32895.0f, step[j], ah[j]);
+              }
             }
           }
+          if (pn > rbase + kHalf) {  // the first half is consumed: refill it with the next words
+            __syncwarp();            // every thread's reads of it are done
+            do {
+              load_half(rbase + kRing);
+              rbase += kHalf;
+            } while (pn > rbase + kHalf);
+          }
+          lim = min(nw, rbase + kHalf);  // all but the refill just issued have landed
+        } else {
+          ring_words();
         }
         p = pn;
-        if (pn > rbase + kHalf) {  // the first half is consumed: refill it with the next words
-          __syncwarp();            // every thread's reads of it are done
-          cp_async_wait_all();     // and the other half has landed before it becomes the first
-          do {
-            load_half(rbase + kRing);
-            rbase += kHalf;
-          } while (pn > rbase + kHalf);
-          lim = min(lim, rbase + kHalf);
-        }
         store_row(v[0], v[1], v[2], v[3]);
         next_row();
       }
