@@ -82,6 +82,8 @@ def lib():
             "orc_encode_stream": (ctypes.c_int64, [P, P, ctypes.c_int64, P, P, P, P, P, P,
                                                    ctypes.c_int64, P, P]),
             "orc_encode_bound": (ctypes.c_uint64, [P]),
+            "orc_table_entropy": (ctypes.c_double, [P]),
+            "orc_container_fixed_bytes": (ctypes.c_uint64, [P]),
             "orc_encode": (ctypes.c_int, [P, ctypes.c_int32, P, P, P, P, ctypes.c_uint64, P, P]),
             "orc_decode": (ctypes.c_int, [P, ctypes.c_size_t, P, ctypes.c_uint64, ctypes.c_int64,
                                           ctypes.c_int64, P]),
@@ -233,8 +235,10 @@ def fit_head(cd: Codec, base, mult, head: np.ndarray):
     return rc, st, rp, cdf
 
 
-def encode_stream(cd: Codec, head, k, step_, recip, cdf):
-    """Encode chunk k of one head -> (rc_or_len, block bytes, s[d], anchors[ng][d])."""
+def encode_stream(cd: Codec, head, k, step_, recip, cdf, symcount=None, stats=None):
+    """Encode chunk k of one head -> (rc_or_len, block bytes, s[d], anchors[ng][d]).
+    symcount (uint64 [d][256]) accumulates the coded symbols per lane's
+    table; stats (Stats) accumulates the stream's size split."""
     head = np.ascontiguousarray(head, np.uint16)
     ntok = min(cd.C, cd.S - k * cd.C)
     ng = -(-ntok // cd.G)
@@ -245,7 +249,7 @@ def encode_stream(cd: Codec, head, k, step_, recip, cdf):
     n = lib().orc_encode_stream(_ref(cd.dims()), _p(head), k, _p(np.ascontiguousarray(step_, np.float32)),
                                 _p(np.ascontiguousarray(recip, np.float32)),
                                 _p(np.ascontiguousarray(cdf, np.uint16)), _p(s), _p(anc), _p(blk), cap,
-                                None, None)
+                                None if symcount is None else _p(symcount), None if stats is None else _ref(stats))
     return n, (blk[:n].copy() if n > 0 else None), s, anc
 
 
@@ -319,6 +323,20 @@ def tables_views(tables: np.ndarray, cd: Codec, n_levels: int):
     recip = tables[o2:o2 + 4 * nc].view(np.float32).reshape(shp)
     cdf = tables[o3:o3 + 512 * nc].view(np.uint16).reshape(shp + (256,))
     return step_, recip, cdf
+
+
+def table_entropy(counts: np.ndarray) -> float:
+    """sum_s n_s log2(N / n_s) (bits) of one table's 256 symbol counts."""
+    c = np.ascontiguousarray(counts, np.uint64)
+    assert c.shape == (256,)
+    return lib().orc_table_entropy(_p(c))
+
+
+def container_fixed_bytes(cd: Codec) -> int:
+    """Header, index and per-chunk fixed parts of a container, unpadded (the
+    structural term of the entropy bound; stream headers are counted per
+    stream by encode_stream's stats)."""
+    return lib().orc_container_fixed_bytes(_ref(cd.dims()))
 
 
 def entropy_bound_bytes(st: Stats, table_bytes: int = 0) -> float:

@@ -641,7 +641,13 @@ uint64_t orc_encode_bound(const orc_dims *dm)
     return total;
 }
 
-static double table_entropy(const uint64_t *n)
+/* Bits the coded symbols of one table carry at their own empirical
+ * frequencies: sum_s n_s log2(N / n_s) over the 256 symbols (escape
+ * included).  Summed over the tables it is the first term of the entropy
+ * bound a container is measured against: the size an ideal coder would
+ * reach with the empirical symbol distribution of each (layer, channel)
+ * table (Guide, pillar 3, "Distribution-Aware Arithmetic Coding"). */
+double orc_table_entropy(const uint64_t *n)
 {
     uint64_t N = 0;
     for (int s = 0; s < 256; s++)
@@ -651,6 +657,21 @@ static double table_entropy(const uint64_t *n)
         if (n[s])
             h += (double)n[s] * log2((double)N / (double)n[s]);
     return h;
+}
+
+/* Information-bearing structure of a container outside its streams, as
+ * the entropy bound counts it (no padding): the header and chunk index, and
+ * per chunk its header, scales, anchors and stream offsets.  Stream headers
+ * (16 bytes each) are counted by orc_encode_stream. */
+uint64_t orc_container_fixed_bytes(const orc_dims *dm)
+{
+    const int64_t nk = n_chunks_of(dm), nstr = (int64_t)dm->L * 2 * dm->H, d = dm->d;
+    uint64_t fixed = 64 + 8 * (uint64_t)nk;
+    for (int64_t k = 0; k < nk; k++) {
+        int64_t ng = ceil_div(chunk_ntok(dm, k), dm->G);
+        fixed += 16 + 4 * (uint64_t)nstr * d + (uint64_t)(nstr * ng * d) + 4 * (uint64_t)nstr;
+    }
+    return fixed;
 }
 
 int orc_encode(const orc_dims *dm, int32_t n_levels, const uint8_t *tables,
@@ -735,14 +756,9 @@ int orc_encode(const orc_dims *dm, int32_t n_levels, const uint8_t *tables,
         if (st) {
             double h = 0.0;
             for (uint64_t i = 0; i < nc; i++)
-                h += table_entropy(cnt + i * 256);
-            uint64_t fixed = 64 + 8 * (uint64_t)nk;
-            for (int64_t k = 0; k < nk; k++) {
-                int64_t ng = ceil_div(chunk_ntok(dm, k), dm->G);
-                fixed += 16 + 4 * (uint64_t)nstr * d + (uint64_t)(nstr * ng * d) + 4 * (uint64_t)nstr;
-            }
+                h += orc_table_entropy(cnt + i * 256);
             local.entropy_bits = h;
-            local.fixed_bytes += fixed;
+            local.fixed_bytes += orc_container_fixed_bytes(dm);
             local.pad_bytes = pos - local.fixed_bytes - local.state_bytes - 2 * local.n_words;
             *st = local;
         }

@@ -122,6 +122,12 @@ int64_t orc_encode_stream(const orc_dims *dm, const uint16_t *head,
                           uint64_t *symcount, orc_stats *st);
 
 uint64_t orc_encode_bound(const orc_dims *dm);
+/* sum_s n_s log2(N/n_s) of one table's 256 symbol counts (bits). */
+double orc_table_entropy(const uint64_t *counts);
+/* Header, chunk index and per-chunk fixed parts of a container, unpadded
+ * (the structural bytes of the entropy bound, stream headers excluded). */
+uint64_t orc_container_fixed_bytes(const orc_dims *dm);
+
 int orc_encode(const orc_dims *dm, int32_t n_levels, const uint8_t *tables,
                const uint16_t *kv, const uint8_t *chunk_level, uint8_t *out,
                uint64_t cap, uint64_t *out_bytes, orc_stats *st);

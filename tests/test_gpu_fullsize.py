@@ -1,15 +1,21 @@
-"""Full-size GPU parity on the four large workloads, by sampled heads.
+"""Full-size GPU parity on the four large workloads, every stream.
 
 The GPU fits, encodes and decodes the whole workload in the launch
-configuration the benchmark uses.  The oracle then recomputes, for three
-heads spread over the layers, everything that depends on them: the fitted
-table rows (every level), every chunk's stream block, scales and int8
-anchors, and the decoded fp16 tokens.  All comparisons are bit-exact.  The
+configuration the benchmark uses.  The oracle then checks, on every host
+core (tests/fullverify.py), every chunk stream of every head: the stream
+block, scales and int8 anchors byte for byte against its own encode with the
+GPU's table rows, the table rows against its own fit, the decoded fp16
+tokens against its own decode of the container's streams, and the chunk
+index and stream offsets against its stream lengths.  Each container is also held to the entropy bound of its
+coded symbols: at most 1% above it (the spec gate of the codec).  The
 long-context mixed-level workload is also decoded chunk group by chunk group
-on a side stream while the next group is copied from pinned host memory,
-and must equal the one-shot decode.
+on a side stream while the next group is copied from pinned host memory, and
+must equal the one-shot decode.
 """
+import json
+import os
 import time
+from multiprocessing import shared_memory
 
 import numpy as np
 import pytest
@@ -17,29 +23,26 @@ import pytest
 from kv_cache_compression_02_gb300 import cachegen as cg
 from kv_cache_compression_02_gb300 import synth
 from kv_cache_compression_02_gb300 import workloads as W
+from tests import fullverify
 from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
 
-def _pad16(v):
-    return (v + 15) // 16 * 16
-
-
-def _sample_heads(w):
-    return [(0, 0, 0), (w.L // 2, 1, w.H // 2), (w.L - 1, 1, w.H - 1)]
-
-
 class Run:
-    """GPU fit + encode (one container per level set) + decode of a workload."""
+    """GPU fit + encode (one container per level set) + decode of a workload;
+    the input KV is generated into host shared memory, which the oracle
+    workers read."""
 
     def __init__(self, w):
         T = gu.torch()
         gu.ready()
         self.w = w
-        self.host = T.empty(w.elements, dtype=T.int16, pin_memory=True)
-        synth.fill(w.gen, self.host.data_ptr())
-        self.kv = self.host.cuda()
+        self.shm = shared_memory.SharedMemory(create=True, size=w.fp16_bytes)
+        host = np.ndarray(w.elements, np.uint16, buffer=self.shm.buf)
+        synth.fill(w.gen, host.ctypes.data)
+        self.kv = T.frombuffer(self.shm.buf, dtype=T.int16, count=w.elements).cuda()
+        del host
         self.cfg = cg.Config.from_workload(w)
         self.tables = cg.empty_u8(cg.cg_tables_bytes(self.cfg))
         ws = cg.empty_u8(cg.cg_workspace_bytes(self.cfg, cg.CG_OP_FIT))
@@ -47,7 +50,10 @@ class Run:
         T.cuda.synchronize()
         assert cg.cg_read_status(ws) == cg.CG_OK
         del ws
-        self.tables_host = self.tables.cpu().numpy()
+
+    def close(self):
+        self.shm.close()
+        self.shm.unlink()
 
     def encode(self, levels):
         T = gu.torch()
@@ -71,84 +77,72 @@ class Run:
         return out
 
 
-def _check_heads(orc, run, cont_host, levels, decoded_dev):
-    w = run.w
-    cd = orc.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
-    step_, recip, cdf = orc.tables_views(run.tables_host, cd, w.n_levels)
-    lm = w.layer_mult_array()
-    hostkv = run.host.numpy().view(np.uint16)
-    nstr = w.L * 2 * w.H
-    chunk_off = cont_host[64:64 + 8 * w.n_chunks].view(np.uint64)
-    for (l, kv, h) in _sample_heads(w):
-        si = (l * 2 + kv) * w.H + h
-        head = hostkv[si * w.S * w.d:(si + 1) * w.S * w.d].reshape(w.S, w.d)
-        mult = lm[l, kv] if lm is not None else [0.5, 1.0, 2.0][(3 * l) // w.L]
-        c0 = h * w.d
-        for lv in range(w.n_levels):
-            rc, st, rp, cf = orc.fit_head(cd, w.level_base[lv], mult, head)
-            assert rc == 0
-            assert np.array_equal(st, step_[lv, l, kv, c0:c0 + w.d]), (l, kv, h, lv)
-            assert np.array_equal(rp, recip[lv, l, kv, c0:c0 + w.d])
-            assert np.array_equal(cf, cdf[lv, l, kv, c0:c0 + w.d])
-        dec_head = decoded_dev[si * w.S * w.d:(si + 1) * w.S * w.d].cpu().numpy().view(np.uint16).reshape(w.S, w.d)
-        ref_head = np.zeros((w.S, w.d), np.uint16)
-        for k in range(w.n_chunks):
-            lv = int(levels[k])
-            ntok = min(w.C, w.S - k * w.C)
-            ng = -(-ntok // w.G)
-            base = int(chunk_off[k])
-            sec_anc = 16 + _pad16(4 * nstr * w.d)
-            sec_off = sec_anc + _pad16(nstr * ng * w.d)
-            so = int(cont_host[base + sec_off + 4 * si: base + sec_off + 4 * si + 4].view(np.uint32)[0])
-            n, blk, s, anc = orc.encode_stream(cd, head, k, step_[lv, l, kv, c0:c0 + w.d],
-                                               recip[lv, l, kv, c0:c0 + w.d], cdf[lv, l, kv, c0:c0 + w.d])
-            assert n > 0
-            assert np.array_equal(cont_host[base + so: base + so + n], blk), (l, kv, h, k)
-            gs = cont_host[base + 16 + 4 * si * w.d: base + 16 + 4 * (si + 1) * w.d].view(np.float32)
-            assert np.array_equal(gs, s)
-            ga = cont_host[base + sec_anc + si * ng * w.d: base + sec_anc + (si + 1) * ng * w.d].view(np.int8)
-            assert np.array_equal(ga.reshape(ng, w.d), anc)
-            rc = orc.decode_stream(cd, cont_host[base + so: base + so + n], k, step_[lv, l, kv, c0:c0 + w.d],
-                                   cdf[lv, l, kv, c0:c0 + w.d], gs, ga.reshape(ng, w.d), ref_head)
-            assert rc == 0
-        assert np.array_equal(dec_head, ref_head), (l, kv, h)
+def _verify(run, cont, levels, decoded, **kw):
+    """Every stream against the oracle; the container within 1% of the
+    entropy bound of its coded symbols.  The report is printed (and appended
+    as a JSON line to the file CG_FULLVERIFY_OUT names, if set)."""
+    t0 = time.time()
+    rep = fullverify.verify(run.w, run.tables, cont, levels, decoded, kv_shm=run.shm.name, **kw)
+    rep["seconds"] = round(time.time() - t0, 1)
+    rep["procs"] = os.cpu_count()
+    line = json.dumps({k: v for k, v in rep.items() if k != "errors"} | {"n_errors": len(rep["errors"])})
+    print("\n" + line)
+    if os.environ.get("CG_FULLVERIFY_OUT"):
+        with open(os.environ["CG_FULLVERIFY_OUT"], "a") as fh:
+            fh.write(line + "\n")
+    assert not rep["errors"], rep["errors"][:20]
+    assert rep["actual_over_bound"] <= 1.01, rep
+    return rep
 
 
 @pytest.mark.parametrize("w", [W.LLAMA7B, W.LLAMA3_70B], ids=lambda w: w.name)
-def test_fullsize_single_level(orc, w):
+def test_fullsize_single_level(w):
     run = Run(w)
-    levels = w.levels_for()
-    cont = run.encode(levels)
-    decoded = run.decode(cont)
-    cont_host = cont.cpu().numpy()
-    assert w.fp16_bytes / cont_host.size > 2.5
-    _check_heads(orc, run, cont_host, levels, decoded)
+    try:
+        levels = w.levels_for()
+        cont = run.encode(levels)
+        decoded = run.decode(cont)
+        assert w.fp16_bytes / cont.numel() > 2.5
+        _verify(run, cont, levels, decoded)
+    finally:
+        run.close()
 
 
-def test_fullsize_three_levels(orc):
+def test_fullsize_three_levels():
     """Llama-3-8B shape: each chunk encoded at all three levels, each
     level's container decoded and checked on its own."""
     w = W.LLAMA3_8B
     run = Run(w)
-    sizes = []
-    for lv in range(w.n_levels):
-        levels = w.levels_for(lv)
-        cont = run.encode(levels)
-        decoded = run.decode(cont)
-        cont_host = cont.cpu().numpy()
-        sizes.append(cont_host.size)
-        _check_heads(orc, run, cont_host, levels, decoded)
-        del decoded, cont
-    assert sizes[0] > sizes[1] > sizes[2]  # coarser steps, smaller streams
+    try:
+        sizes = []
+        for lv in range(w.n_levels):
+            levels = w.levels_for(lv)
+            cont = run.encode(levels)
+            decoded = run.decode(cont)
+            sizes.append(cont.numel())
+            _verify(run, cont, levels, decoded, tables_every=1 if lv == 0 else 1 << 30)
+            del decoded, cont
+        assert sizes[0] > sizes[1] > sizes[2]  # coarser steps, smaller streams
+    finally:
+        run.close()
 
 
-def test_fullsize_mixed_levels_streamed(orc):
+def test_fullsize_mixed_levels_streamed():
     """Long context, one of four levels per chunk; decoded in chunk groups on
     a side stream overlapped with the next group's host-to-device copy."""
     T = gu.torch()
     w = W.LONGCTX_MIXED
     run = Run(w)
     levels = w.levels_for()
+    try:
+        _streamed(run, levels)
+    finally:
+        run.close()
+
+
+def _streamed(run, levels):
+    T = gu.torch()
+    w = run.w
     cont = run.encode(levels)
     n = cont.numel()
     cont_host = T.empty(n, dtype=T.uint8, pin_memory=True)
@@ -207,4 +201,5 @@ def test_fullsize_mixed_levels_streamed(orc):
         print(f"streamed decode of {w.n_chunks} chunks in groups of {group}: {t * 1e3:.1f} ms "
               f"({w.fp16_bytes / t / 1e9:.0f} GB/s of fp16); overlap efficiency max(copy, decode) / streamed "
               f"= {max(t_copy, t_dec) / t:.2f}")
-    _check_heads(orc, run, ch, levels, out)
+    del dev, cont_host
+    _verify(run, cont, levels, out)

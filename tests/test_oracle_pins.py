@@ -543,3 +543,51 @@ def test_outlier_channel_does_not_touch_other_channels(orc):
     mask = np.ones(dx.shape, bool)
     mask[0, 0, 1, :, 5] = False
     assert np.array_equal(dx[mask], dy[mask])
+
+
+def test_table_entropy_closed_forms(orc):
+    """sum_s n_s log2(N / n_s): uniform counts give N log2(k); two symbols
+    split p, 1-p give N H2(p); an empty or one-symbol table carries 0 bits."""
+    n = np.zeros(256, np.uint64)
+    assert orc.table_entropy(n) == 0.0
+    n[127] = 1000
+    assert orc.table_entropy(n) == 0.0
+    n[:] = 0
+    n[:16] = 5
+    assert abs(orc.table_entropy(n) - 80 * 4.0) < 1e-9
+    n[:] = 0
+    n[3], n[250] = 1, 3
+    h2 = -(0.25 * np.log2(0.25) + 0.75 * np.log2(0.75))
+    assert abs(orc.table_entropy(n) - 4 * h2) < 1e-12
+
+
+def test_per_stream_accounting_adds_up_to_the_container(orc):
+    """Encoding stream by stream with the per-table symbol counts and the
+    size split reproduces orc_encode's statistics of the whole container: the
+    entropy term (summed per table), escapes, words, flush and the structural
+    bytes (container part plus 16 per stream).  This is how the full-size
+    parity pass bounds the GPU's containers stream by stream."""
+    spec = synth.GenSpec(L=2, H=2, d=16, S=700, seed=3, innov="t3", rho=(0.85, 0.99), n_outliers=1,
+                         outlier_scale=20.0)
+    levels, chunk_levels = (0.05, 0.2), [0, 1, 1, 0, 1, 0]
+    x, y, tb, cont, st, cd, lv = _roundtrip(orc, spec, C=128, G=10, levels=levels, chunk_levels=chunk_levels,
+                                            R=20)
+    step_, recip, cdf = orc.tables_views(tb, cd, len(levels))
+    acc = orc.Stats()
+    h = 0.0
+    nstr = spec.L * 2 * spec.H
+    for si in range(nstr):
+        l, kv, hh = si // (2 * spec.H), (si // spec.H) % 2, si % spec.H
+        c0 = hh * spec.d
+        counts = np.zeros((len(levels), spec.d, 256), np.uint64)
+        for k in range(cd.n_chunks):
+            v = lv[k]
+            n, blk, s, anc = orc.encode_stream(cd, x[l, kv, hh], k, step_[v, l, kv, c0:c0 + spec.d],
+                                               recip[v, l, kv, c0:c0 + spec.d], cdf[v, l, kv, c0:c0 + spec.d],
+                                               symcount=counts[v], stats=acc)
+            assert n > 0
+        h += sum(orc.table_entropy(counts[v, j]) for v in range(len(levels)) for j in range(spec.d))
+    assert acc.n_esc == st.n_esc and acc.n_esc > 0
+    assert acc.n_words == st.n_words and acc.n_symbols == st.n_symbols and acc.state_bytes == st.state_bytes
+    assert acc.fixed_bytes + orc.container_fixed_bytes(cd) == st.fixed_bytes
+    assert abs(h - st.entropy_bits) <= 1e-9 * st.entropy_bits
