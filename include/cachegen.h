@@ -69,7 +69,11 @@ typedef enum {
     CG_ERR_CAPACITY = 3,    /* output or workspace too small              */
     CG_ERR_CORRUPT = 4,     /* container or tables failed validation      */
     CG_ERR_CUDA = 5,        /* a CUDA launch or copy failed               */
-    CG_ERR_TIMEOUT = 6      /* reserved: no call waits on another agent   */
+    CG_ERR_TIMEOUT = 6      /* a bulk copy of cg_fit_tables' moment pass
+                               did not land within its bounded wait: the
+                               memory system failed, and the copy may still
+                               land later in shared memory given to other
+                               work, so treat the CUDA context as unusable */
 } cg_status;
 
 typedef struct {
@@ -93,15 +97,23 @@ typedef struct {
 
 enum { CG_OP_FIT = 0, CG_OP_ENCODE = 1, CG_OP_DECODE = 2, CG_OP_ASSEMBLE = 3 };
 
-/* Size in bytes of the tables blob for (dims, params).  0 on bad input. */
+/* Size in bytes of the tables blob for (dims, params): the per-(level,
+ * layer, K/V, channel) quantisation steps and 16-bit CDF tables that the
+ * encoder and decoder share (Guide to CacheGen, pillar 3: frequency tables
+ * per layer and head from calibration profiling; gptget summary of arXiv
+ * 2310.07240, Methodology: per-layer/channel statistics).  0 on bad input. */
 size_t cg_tables_bytes(const cg_dims *dims, const cg_params *params);
 
 /* Workspace bytes needed by operation `op` (CG_OP_*).  0 on bad input.
- * Encode needs about the fp16 size of the KV (word scratch); fit and
- * decode need a few bytes per chunk and channel. */
+ * Encode needs about the fp16 size of the KV (word scratch for the chunk
+ * streams the pages' encoder produces: gptget summary, Methodology, chunked
+ * bitstreams); fit and decode need a few bytes per chunk and channel.  The
+ * caller allocates it; the library allocates nothing. */
 size_t cg_workspace_bytes(const cg_dims *dims, const cg_params *params, int op);
 
-/* Largest container cg_encode can produce for these dims.  With the full
+/* Largest container cg_encode can produce for these dims (the container
+ * format above: the chunked bitstream with its stream-offset index that the
+ * pages' encoder emits, gptget summary, Methodology).  With the full
  * alphabet (alphabet_radius 127) every stream holds at most one 16-bit word
  * per delta symbol, escapes included: a stream that would need more (more
  * than its raw fp16 size) is rejected with CG_ERR_CAPACITY.  So the bound
@@ -111,7 +123,12 @@ size_t cg_workspace_bytes(const cg_dims *dims, const cg_params *params, int op);
  * error. */
 cg_status cg_encode_bound(const cg_dims *dims, const cg_params *params, uint64_t *max_bytes);
 
-/* Fit the tables: per (layer, K/V, channel) sigma over all S tokens (exact
+/* Fit the tables (Guide to CacheGen, pillar 3, "Distribution-Aware
+ * Arithmetic Coding": empirical frequency tables for each layer and head
+ * from calibration profiling; gptget summary of arXiv 2310.07240,
+ * Methodology: statistics per layer and channel; pillar 1, "Layer
+ * Sensitivity Disparity": coarser steps in deeper layers).  Computed here:
+ * per (layer, K/V, channel) sigma over all S tokens (exact
  * integer moments, rounded once), step = max(b*m*sigma, 2^-12) and its
  * reciprocal per level, and per (level, layer, K/V, channel) the 256-bin
  * histogram of the delta symbols over all chunks, normalised to 16-bit
@@ -124,7 +141,12 @@ cg_status cg_encode_bound(const cg_dims *dims, const cg_params *params, uint64_t
 cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void *kv_dev,
                         void *tables_dev, void *ws_dev, size_t ws_bytes, void *stream);
 
-/* Encode kv into a container (format above), chunk k at level
+/* Encode kv into a container (format above): per chunk and head, int8
+ * anchor tokens with the other tokens delta-coded against them (Guide to
+ * CacheGen, pillar 2, "Anchor-Based Delta Encoding"), deltas quantised with
+ * the layer-adaptive step (pillar 1) and range coded with the per-channel
+ * tables (pillar 3; gptget summary, Methodology: delta encoding plus
+ * arithmetic coding into compact bitstreams); chunk k at level
  * chunk_level_host[k] (host array of n_chunks bytes, < n_levels).
  *   out_dev:       out_capacity bytes; on success the first *out_bytes_dev
  *                  bytes are the container (bit-identical to the oracle's).
@@ -164,7 +186,11 @@ cg_status cg_assemble(const cg_dims *dims, const cg_params *params, const void *
 
 /* Decode chunks [chunk_begin, chunk_end) of a container into the full KV
  * buffer kv_dev (fp16 [L][2][H][S][d]; only those chunks' tokens are
- * written).  chunk_end = -1 means all chunks.  dims/params must be the
+ * written): the range decode, anchor + dequantised delta per token, that
+ * turns the received bitstream back into KV "in real time, synchronized
+ * with transmission" (gptget summary of arXiv 2310.07240, Methodology;
+ * Guide to CacheGen, Step 2 decode_sequence and pillar 4, chunk i decoded
+ * while chunk i+1 is in flight).  chunk_end = -1 means all chunks.  dims/params must be the
  * ones the container was made with (the kernel checks them against the
  * container header).  The container must be bitstream_bytes long and the
  * caller must keep it and the tables alive until the stream reaches the
@@ -293,11 +319,15 @@ cg_status cg_simulate_stream(int32_t n_chunks, int32_t n_levels, const uint64_t 
                              const double *decode_s, double *timeline_out, double *total_s_out);
 
 /* Status of the last call that used this workspace (blocking read of the
- * device status word; synchronise the call's stream first). */
+ * device status word; synchronise the call's stream first).  It reports the
+ * device-side checks of the container format above (no passage of the pages
+ * covers error reporting; this is the library's own contract). */
 cg_status cg_read_status(const void *ws_dev);
 
 /* The device address of host memory that is pinned and mapped into the
- * device's address space (cudaHostAlloc, or cudaHostRegister with
+ * device's address space (a helper for the host-resident decode that lets
+ * the decoder read a streamed container as it lands, Guide to CacheGen,
+ * pillar 4; the pages have no call of their own for it) (cudaHostAlloc, or cudaHostRegister with
  * cudaHostRegisterMapped), for the host-resident decode described at
  * cg_decode.  *dev_ptr receives it (NULL on error).  Errors:
  * CG_ERR_INVALID_ARG when host_ptr is not in page-locked host memory
@@ -305,10 +335,12 @@ cg_status cg_read_status(const void *ws_dev);
  * Host only; it launches nothing. */
 cg_status cg_host_mapped(const void *host_ptr, void **dev_ptr);
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string; part of the
+ * library's own error contract, no counterpart in the pages). */
 const char *cg_status_str(cg_status status);
 
-/* Library ABI version (1). */
+/* Library ABI version (1): the version of this header and of the tables
+ * and container formats above (no counterpart in the pages). */
 int32_t cg_version(void);
 
 #ifdef __cplusplus

@@ -169,7 +169,15 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     __syncthreads();  // the stage has been read: it can take the next tile
     if (threadIdx.x == 0 && t + kStatsStages < ntiles) issue(t + kStatsStages);
   }
-  if (s_timeout) {  // a copy never completed: wait (bounded) for the ones in flight, then give up
+  // A copy that has not landed after 2^22 try_wait rounds: every tile is an
+  // in-bounds, 16-byte aligned read of the caller's kv, which completes
+  // unless the memory system itself has failed.  The CTA sets the TIMEOUT
+  // bit, waits (bounded again) for each copy it still has in flight and
+  // returns.  A copy still in flight after that cannot be cancelled: it may
+  // land later in shared memory the SM has since given to another CTA, so
+  // CG_ERR_TIMEOUT tells the caller that the context can no longer be
+  // trusted (the header says so), not merely that the tables are invalid.
+  if (s_timeout) {
     if (threadIdx.x == 0) {
       atomicOr(status, kStTimeout);
       for (uint64_t u = t; u < ntiles && u < t + kStatsStages; u++)
