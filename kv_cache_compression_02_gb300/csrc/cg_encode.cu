@@ -247,6 +247,192 @@ k_encode(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
   }
 }
 
+// ---------------------------------------------------------------- d = 128
+// k_encode for d = 128 (the models' head dim) with the token loop cut down
+// to what a symbol needs: tokens run in reverse over the groups (the anchor
+// rows are not coded), the next row loaded while the current one is coded;
+// each lane quantises, looks up (cdf, f) and takes one rANS step without a
+// branch; one warp vote per token sends a token with an escape to the
+// general path; the suffix shuffle scan uses the shuffle's own range
+// predicate; a thread's words go to their ring slots from one prefix.
+constexpr int kEncTeams128 = 24;
+
+// Inclusive suffix scan step over the warp: v += (value of lane i + O, when
+// there is one).
+template <int O>
+__device__ __forceinline__ uint32_t suffix_step(uint32_t v) {
+  asm("{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+      "shfl.sync.down.b32 t|p, %0, %1, 31, -1;\n\t"
+      "@p add.u32 %0, %0, t;\n\t}"
+      : "+r"(v) : "n"(O));
+  return v;
+}
+
+__global__ void __launch_bounds__(kEncTeams128 * 32, 1)
+k_enc128(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv, uint8_t *ws) {
+  constexpr int T = 32;
+  extern __shared__ __align__(16) uint32_t etab[];  // [256][4][32] : cdf | f << 16, then the word rings
+  const int lv = blockIdx.x, si = blockIdx.y;
+  const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+  const int32_t *counts = reinterpret_cast<const int32_t *>(ws + w.levels);
+  const int32_t *lists = counts + kMaxLevels;
+  const int cnt = counts[lv];
+  if (cnt == 0) return;
+  uint32_t *status = reinterpret_cast<uint32_t *>(ws + w.status);
+
+  const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
+                        tab_index(lo, lv, l, kvi, h * lo.d) * 256;
+  for (int e = threadIdx.x; e < 128 * 256; e += blockDim.x) {
+    const int c = e >> 8, s = e & 255;
+    const uint32_t c0 = cdf[c * 256 + s];
+    const uint32_t c1 = s < 255 ? cdf[c * 256 + s + 1] : kM;
+    etab[(s * kLpt + (c % kLpt)) * T + c / kLpt] = c0 | ((c1 - c0) << 16);
+  }
+  __syncthreads();
+
+  const int team = threadIdx.x >> 5, nteams = blockDim.x >> 5;
+  const uint32_t i = threadIdx.x & 31;
+  uint16_t *ring = reinterpret_cast<uint16_t *>(etab + 256 * 128) + team * kWordRing;
+  const uint32_t *et = etab + i;  // thread i's entries: et[(sym * 4 + j) * 32]
+  const float4 rc4 = *reinterpret_cast<const float4 *>(
+      reinterpret_cast<const float *>(tables + lo.tb_recip) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
+  const float rc[4] = {rc4.x, rc4.y, rc4.z, rc4.w};
+  const int R = lo.R;
+
+  for (int idx = team; idx < cnt; idx += nteams) {
+    const int k = lists[lv * lo.n_chunks + idx];
+    const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k);
+    const int64_t t0 = int64_t(k) * lo.C;
+    const uint8_t *chunk = ws + w.chunks + uint64_t(k) * lo.fixed_full;
+    const float4 s4 = *reinterpret_cast<const float4 *>(chunk + lo.sec_s + (uint64_t(si) * lo.d + kLpt * i) * 4);
+    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint8_t *anc = chunk + lo.sec_anc + uint64_t(si) * ng * lo.d + kLpt * i;
+    const uint16_t *xin = kv + (uint64_t(si) * lo.S + t0) * lo.d + kLpt * i;
+    const uint64_t sidx = uint64_t(k) * lo.nstr + si;
+    uint16_t *wout = reinterpret_cast<uint16_t *>(ws + w.words) + sidx * w.words_cap;
+    const int64_t cap = int64_t(w.words_cap);
+
+    uint32_t x[4] = {kRansL, kRansL, kRansL, kRansL};
+    int64_t E = 0;  // words emitted so far (encoder order)
+    uint32_t nesc = 0, badm = 0;
+    bool overflow = false;
+    // the first token coded: the chunk's last delta token (none when every
+    // token is an anchor)
+    int g = ng - 1;
+    int tt = min(lo.G, ntok - g * lo.G) - 1;  // its place in group g
+    if (tt < 1 && g > 0) {
+      g--;
+      tt = lo.G - 1;
+    }
+    uint2 cur = tt >= 1 ? __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(g * lo.G + tt) * lo.d))
+                        : make_uint2(0, 0);
+    for (; g >= 0 && tt >= 1 && !overflow; g--, tt = lo.G - 1) {
+      const uint32_t a4 = *reinterpret_cast<const uint32_t *>(anc + uint64_t(g) * lo.d);
+      float ah[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) ah[j] = __fmul_rn(float(int8_t(a4 >> (8 * j))), sc[j]);
+      for (; tt >= 1; tt--) {
+        // the next token coded: t - 1, or across this group's anchor t - 2
+        const int t = g * lo.G + tt;
+        const int tn = tt > 1 ? t - 1 : t - 2;
+        const uint2 raw = cur;
+        if (tn >= 1) cur = __ldg(reinterpret_cast<const uint2 *>(xin + int64_t(tn) * lo.d));
+        badm |= ((raw.x & 0x7C007C00u) + 0x04000400u) | ((raw.y & 0x7C007C00u) + 0x04000400u);
+        const uint32_t hw[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+        uint32_t word[4], qv[4];
+        bool esc[4], ren[4];
+        uint32_t cntw = 0;
+#pragma unroll
+        for (int j = 3; j >= 0; j--) {
+          const float xv = __half2float(__ushort_as_half(uint16_t(hw[j])));
+          const int q = __float2int_rn(__fmul_rn(__fsub_rn(xv, ah[j]), rc[j]));
+          esc[j] = uint32_t(q) + uint32_t(R) > uint32_t(2 * R);  // |q| > R, in unsigned arithmetic
+          const int sym = esc[j] ? kEsc : q + 127;
+          const uint32_t e = et[(sym * kLpt + j) * T];
+          const uint32_t f = e >> 16, c = e & 0xFFFFu;
+          ren[j] = x[j] >= (f << 16);
+          word[j] = x[j] & 0xFFFFu;
+          x[j] = rans_put(ren[j] ? (x[j] >> 16) : x[j], f, c);
+          qv[j] = uint32_t(q);
+          cntw += ren[j] ? 1u : 0u;
+        }
+        const bool esc_warp = __any_sync(0xffffffffu, esc[0] | esc[1] | esc[2] | esc[3]);
+        if (esc_warp) cntw += 2 * ((esc[0] ? 1u : 0u) + (esc[1] ? 1u : 0u) + (esc[2] ? 1u : 0u) + (esc[3] ? 1u : 0u));
+        // emission order: lanes descending, i.e. threads descending
+        uint32_t suf = suffix_step<1>(cntw);
+        suf = suffix_step<2>(suf);
+        suf = suffix_step<4>(suf);
+        suf = suffix_step<8>(suf);
+        suf = suffix_step<16>(suf);
+        const uint32_t tot = __shfl_sync(0xffffffffu, suf, 0);
+        if (E + tot > cap) {
+          overflow = true;
+          break;
+        }
+        // word e of the stream (encoder order) goes to ring slot ~e mod the
+        // ring size, so a block of 256 words sits in the ring in the order it
+        // takes at the end of the scratch slot (which is filled backwards)
+        const uint32_t e0 = uint32_t(E), e = e0 + suf - cntw;
+        if (!esc_warp) {
+          const uint32_t p2 = e + (ren[3] ? 1u : 0u), p1 = p2 + (ren[2] ? 1u : 0u), p0 = p1 + (ren[1] ? 1u : 0u);
+          if (ren[3]) ring[~e & (kWordRing - 1)] = uint16_t(word[3]);
+          if (ren[2]) ring[~p2 & (kWordRing - 1)] = uint16_t(word[2]);
+          if (ren[1]) ring[~p1 & (kWordRing - 1)] = uint16_t(word[1]);
+          if (ren[0]) ring[~p0 & (kWordRing - 1)] = uint16_t(word[0]);
+        } else {  // escapes: the raw q follows the word (decode order: word, low half, high half)
+          uint32_t ee = e;
+#pragma unroll
+          for (int j = 3; j >= 0; j--) {
+            if (esc[j]) {
+              ring[~ee & (kWordRing - 1)] = uint16_t(qv[j] >> 16);
+              ring[~(ee + 1) & (kWordRing - 1)] = uint16_t(qv[j] & 0xFFFFu);
+              ee += 2;
+              nesc++;
+            }
+            if (ren[j]) {
+              ring[~ee & (kWordRing - 1)] = uint16_t(word[j]);
+              ee += 1;
+            }
+          }
+        }
+        const uint32_t e1 = e0 + tot;
+        if ((e1 >> 8) != (e0 >> 8)) {  // blocks completed: 16-byte stores into the slot
+          __syncwarp();
+          for (uint32_t blk = e0 >> 8; blk < (e1 >> 8); blk++) flush_block(ring, wout, cap, blk, 0, int(i), T);
+          __syncwarp();  // the block's reads are done before its slots take new words
+        }
+        E += tot;
+      }
+    }
+    const bool bad = (badm & 0x80008000u) != 0;
+    if (!overflow && (E & 255)) {  // the last, partial block: only units that hold its words
+      __syncwarp();
+      const uint32_t blk = uint32_t(E) >> 8;
+      flush_block(ring, wout, cap, blk, (256 * (blk + 1) - uint32_t(E)) / 8, int(i), T);
+    }
+    if (bad) atomicOr(status, kStNonfinite);
+    if (overflow) {
+      if (i == 0) atomicOr(status, kStCapacity);
+      continue;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) nesc += __shfl_xor_sync(0xffffffffu, nesc, o);
+    if (i == 0) reinterpret_cast<uint2 *>(ws + w.info)[sidx] = make_uint2(uint32_t(E), nesc);
+    reinterpret_cast<uint4 *>(ws + w.states)[(sidx * lo.d) / 4 + i] = make_uint4(x[0], x[1], x[2], x[3]);
+  }
+}
+
+cudaError_t launch_encode_128(const Layout &lo, const EncWs &w, const uint8_t *tables, const uint16_t *kv,
+                              uint8_t *ws, int teams, cudaStream_t st) {
+  if (teams > kEncTeams128) teams = kEncTeams128;
+  const size_t smem = size_t(256) * 128 * 4 + size_t(teams) * kWordRing * 2;
+  cudaError_t e = cudaFuncSetAttribute(k_enc128, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, lo.nstr);
+  k_enc128<<<grid, teams * 32, smem, st>>>(lo, w, tables, kv, ws);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- scans
 constexpr int kScanThreads = 1024;
 
@@ -473,7 +659,7 @@ cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *table
     case 4: return launch_encode_t<4>(lo, w, tables, kv, ws, teams, st);
     case 8: return launch_encode_t<8>(lo, w, tables, kv, ws, teams, st);
     case 16: return launch_encode_t<16>(lo, w, tables, kv, ws, teams, st);
-    case 32: return launch_encode_t<32>(lo, w, tables, kv, ws, teams, st);
+    case 32: return launch_encode_128(lo, w, tables, kv, ws, teams, st);
     default: return cudaErrorInvalidValue;
   }
 }
