@@ -160,32 +160,37 @@ def generate_pinned(w, torch):
 
 def cpu_oracle_decode_rate(w, host_np, budget_s=10.0):
     """Single-threaded oracle decode rate (fp16 bytes/s) on a bounded sample:
-    chunk-0 streams of successive heads, each fitted and encoded by the
-    oracle first (untimed), until budget_s of decode time has been spent."""
+    the chunk streams of successive heads, each fitted by the oracle first
+    (untimed) and encoded (timed apart: the oracle's encode rate), until
+    budget_s of decode time has been spent.  Returns (decode rate, decode
+    seconds, streams, encode rate)."""
     import oracle
     oracle.build()
     cd = oracle.Codec(w.L, w.H, w.d, w.S, w.C, w.G, w.R)
     L, H, S, d = w.L, w.H, w.S, w.d
-    spent, nbytes, streams = 0.0, 0, 0
+    spent, spent_enc, nbytes, streams = 0.0, 0.0, 0, 0
     heads = L * 2 * H
     step_ = max(1, heads // 128)
     out = np.zeros((S, d), np.uint16)
+    lm = w.layer_mult_array()
     for si in range(0, heads, step_):
-        l = si // (2 * H)
+        l, kvi = si // (2 * H), (si // H) % 2
         head = host_np[si * S * d:(si + 1) * S * d].reshape(S, d)
-        m = [0.5, 1.0, 2.0][(3 * l) // L]
+        m = lm[l, kvi] if lm is not None else [0.5, 1.0, 2.0][(3 * l) // L]
         rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
         for k in range(cd.n_chunks):
-            n, blk, s, anc = oracle.encode_stream(cd, head, k, st, rp, cdf)
             t0 = time.perf_counter()
+            n, blk, s, anc = oracle.encode_stream(cd, head, k, st, rp, cdf)
+            t1 = time.perf_counter()
             rc = oracle.decode_stream(cd, blk, k, st, cdf, s, anc, out)
-            spent += time.perf_counter() - t0
+            spent += time.perf_counter() - t1
+            spent_enc += t1 - t0
             assert rc == 0
             nbytes += min(w.C, S - k * w.C) * d * 2
             streams += 1
             if spent >= budget_s:
-                return nbytes / spent, spent, streams
-    return nbytes / spent, spent, streams
+                return nbytes / spent, spent, streams, nbytes / spent_enc
+    return nbytes / spent, spent, streams, nbytes / spent_enc
 
 
 def _oracle_worker(args):
@@ -204,7 +209,8 @@ def _oracle_worker(args):
     for si in range(first, w.L * 2 * w.H, stride):
         l, kv, h = si // (2 * w.H), (si // w.H) % 2, si % w.H
         head = synth.head(w.gen, l, kv, h)
-        m = [0.5, 1.0, 2.0][(3 * l) // w.L]
+        lm = w.layer_mult_array()
+        m = lm[l, kv] if lm is not None else [0.5, 1.0, 2.0][(3 * l) // w.L]
         rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
         for k in range(cd.n_chunks):
             n, blk, sc, anc = oracle.encode_stream(cd, head, k, st, rp, cdf)
@@ -232,7 +238,9 @@ def cpu_oracle_decode_rate_all_cores(name, budget_s=10.0):
 def workload_config(w, world):
     """The bench line's config for workload w (both arms)."""
     return {"workload": w.name, "L": w.L, "H_kv": w.H, "d": w.d, "S": w.S, "C": w.C, "G": w.G,
-            "levels": list(w.level_base), "fp16_bytes": w.fp16_bytes, "l2": "inputs larger than L2 (10.7 GB)",
+            "levels": list(w.level_base), "chunk_levels": w.chunk_levels, "fp16_bytes": w.fp16_bytes,
+            "l2": (f"inputs larger than L2 ({w.fp16_bytes / 1e9:.1f} GB)" if 2 * w.fp16_bytes >= (256 << 20)
+                   else "a 256 MB buffer written between steps (inputs smaller than L2)"),
             "parallelism": f"independent replica per GPU x{world}"}
 
 
@@ -257,7 +265,9 @@ def _ref_init(name, nworkers, per_worker, ids):
         si = ((widx % nworkers) + j * nworkers) * stride % nsi
         l, kv, h = si // (2 * w.H), (si // w.H) % 2, si % w.H
         head = synth.head(w.gen, l, kv, h)
-        rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], [0.5, 1.0, 2.0][(3 * l) // w.L], head)
+        lm = w.layer_mult_array()
+        m = lm[l, kv] if lm is not None else [0.5, 1.0, 2.0][(3 * l) // w.L]
+        rc, st, rp, cdf = oracle.fit_head(cd, w.level_base[0], m, head)
         n, blk, sc, anc = oracle.encode_stream(cd, head, 0, st, rp, cdf)
         prepared.append((blk, st, cdf, sc, anc))
     _REF = (cd, np.zeros((w.S, w.d), np.uint16), prepared)
@@ -340,36 +350,48 @@ def main():
     ws_fit = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_FIT))
     ws_enc = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_ENCODE))
     ws_dec = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_DECODE))
-    out = cg.empty_u8(cg.cg_encode_bound(cfg))
+    # the containers a step encodes and decodes: one, or (for a workload
+    # coded once per level) one per level
+    level_sets = ([w.levels_for(v) for v in range(w.n_levels)] if w.chunk_levels == "each"
+                  else [w.levels_for()])
+    nsets = len(level_sets)
+    outs = [cg.empty_u8(cg.cg_encode_bound(cfg)) for _ in level_sets]
+    out = outs[0]
     nbytes_d = torch.zeros(1, dtype=torch.int64, device=dev)
     kv_out = torch.empty_like(kv)
-    levels = w.levels_for()
+    levels = level_sets[0]
+    # inputs smaller than L2: a buffer larger than L2 is written between steps
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if 2 * w.fp16_bytes < (256 << 20) else None
     torch.cuda.synchronize()
 
-    ev = {k: [] for k in ("fit", "enc", "dec")}
-    nbytes = None
+    ev = {"fit": [], "enc": [[] for _ in level_sets], "dec": [[] for _ in level_sets]}
+    nbytes_list = [None] * nsets
 
     def step(record: bool):
-        nonlocal nbytes
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * nsets)]
         e[0].record(stream)
         cg.check(cg.cg_fit_tables(cfg, kv, tables, ws_fit, stream), "cg_fit_tables")
         e[1].record(stream)
-        cg.check(cg.cg_encode(cfg, tables, kv, levels, out, nbytes_d, ws_enc, stream), "cg_encode")
-        e[2].record(stream)
-        if nbytes is None:
-            torch.cuda.synchronize()
-            nbytes = int(nbytes_d.item())
-        cg.check(cg.cg_decode(cfg, tables, out, nbytes, 0, -1, kv_out, ws_dec, stream), "cg_decode")
-        e[3].record(stream)
+        for j, lv_set in enumerate(level_sets):
+            cg.check(cg.cg_encode(cfg, tables, kv, lv_set, outs[j], nbytes_d, ws_enc, stream), "cg_encode")
+            e[2 + 2 * j].record(stream)
+            if nbytes_list[j] is None:
+                torch.cuda.synchronize()
+                nbytes_list[j] = int(nbytes_d.item())
+            cg.check(cg.cg_decode(cfg, tables, outs[j], nbytes_list[j], 0, -1, kv_out, ws_dec, stream), "cg_decode")
+            e[3 + 2 * j].record(stream)
         if record:
             ev["fit"].append((e[0], e[1]))
-            ev["enc"].append((e[1], e[2]))
-            ev["dec"].append((e[2], e[3]))
+            for j in range(nsets):
+                ev["enc"][j].append((e[1 + 2 * j], e[2 + 2 * j]))
+                ev["dec"][j].append((e[2 + 2 * j], e[3 + 2 * j]))
+        if l2_flush is not None:
+            l2_flush.zero_()
 
     for _ in range(max(args.warmup, 1)):
         step(False)
     torch.cuda.synchronize()
+    nbytes = nbytes_list[0]
     for ws, what in ((ws_fit, "fit"), (ws_enc, "encode"), (ws_dec, "decode")):
         cg.check(cg.cg_read_status(ws), what)
     # sanity: the decode reproduces the input within the quantization error
@@ -377,6 +399,9 @@ def main():
     ys = kv_out[: 1 << 20].view(torch.float16).float()
     if not torch.isfinite(ys).all() or (xs - ys).abs().max().item() > 0.5 * xs.abs().max().item():
         raise RuntimeError("decoded KV does not match the input")
+    # the entropy bound of each single-level container, from the fit's histograms
+    ebounds = [cg.cg_entropy_bound(cfg, ws_fit, int(s_[0])) if len(set(s_.tolist())) == 1 else None
+               for s_ in level_sets]
 
     clocks = Clocks(local)
     clocks.start()
@@ -393,8 +418,13 @@ def main():
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms_step = t_start.elapsed_time(t_end) / args.steps
-    ms = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    mean_ms = lambda v: sum(a.elapsed_time(b) for a, b in v) / len(v)  # noqa: E731
+    ms_enc_sets = [mean_ms(v) for v in ev["enc"]]
+    ms_dec_sets = [mean_ms(v) for v in ev["dec"]]
+    ms = {"fit": mean_ms(ev["fit"]), "enc": sum(ms_enc_sets), "dec": sum(ms_dec_sets)}
+    # the steps' own time (the L2 flush between steps, when there is one, excluded)
+    ms_step = (t_start.elapsed_time(t_end) / args.steps if l2_flush is None
+               else ms["fit"] + ms["enc"] + ms["dec"])
     for ws, what in ((ws_fit, "fit"), (ws_enc, "encode"), (ws_dec, "decode")):
         cg.check(cg.cg_read_status(ws), what)
 
@@ -606,12 +636,12 @@ def main():
         [ms["dec"], ms["enc"], ms["fit"], ms_step, statistics.mean(e2e_ms), statistics.mean(e2e_pipe_ms),
          statistics.mean(e2e_serial_ms)], world, dev)
     fp16 = w.fp16_bytes
-    dec_gbs = job_gbs(fp16, world, ms_dec)
-    enc_gbs = job_gbs(fp16, world, ms_enc)
+    dec_gbs = job_gbs(nsets * fp16, world, ms_dec)
+    enc_gbs = job_gbs(nsets * fp16, world, ms_enc)
     fit_gbs = job_gbs(fp16, world, ms_fit)
     peak, peak_kind = peaks()
-    dec_alg = nbytes + fp16
-    enc_alg = fp16 + nbytes
+    dec_alg = sum(nbytes_list) + nsets * fp16
+    enc_alg = nsets * fp16 + sum(nbytes_list)
     dec_ach = dec_alg / (ms["dec"] * 1e-3) / 1e9
     enc_ach = enc_alg / (ms["enc"] * 1e-3) / 1e9
     tb_bytes = tables.numel()
@@ -624,13 +654,14 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        rate, spent, nstreams = cpu_oracle_decode_rate(w, host.numpy().view(np.uint16), budget_s=8.0)
+        rate, spent, nstreams, rate_enc = cpu_oracle_decode_rate(w, host.numpy().view(np.uint16), budget_s=8.0)
         rate_all, cores = cpu_oracle_decode_rate_all_cores(w.name, budget_s=8.0)
         cpu = {"value": rate_all / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"oracle decode of chunk streams ({w.C} tokens x {w.d} lanes) of heads spread over the "
                          f"layers, one process per core, 8 s of decode each",
                "single_core": {"value": rate / 1e9, "unit": "GB/s", "cores": 1,
-                               "sample": f"{nstreams} streams, {spent:.1f} s"}}
+                               "encode_gbs": rate_enc / 1e9,
+                               "sample": f"{nstreams} streams, {spent:.1f} s of decode (encode timed apart)"}}
     line = {
         "metric": METRIC, "value": dec_gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
@@ -640,6 +671,16 @@ def main():
         "ms": {"fit": ms_fit, "encode": ms_enc, "decode": ms_dec},
         "ratio": fp16 / nbytes, "ratio_incl_tables": fp16 / (nbytes + tb_bytes),
         "container_bytes": nbytes, "tables_bytes": tb_bytes,
+        "entropy_bound": {"bound_bytes": ebounds[0], "actual_over_bound": nbytes / ebounds[0] if ebounds[0] else None,
+                          "what": "the container against sum over the (layer, K/V, channel) tables of n log2(N/n) "
+                                  "/ 8 of its coded symbols + 4 bytes per escape + its structural bytes "
+                                  "(cg_entropy_bound, from the fit's histograms); null for a mixed-level container"},
+        "per_level": [{"levels": sorted(set(int(v) for v in s_)), "container_bytes": nb_,
+                       "ratio": fp16 / nb_, "ratio_incl_tables": fp16 / (nb_ + tb_bytes),
+                       "actual_over_bound": nb_ / b_ if b_ else None, "encode_ms": me, "decode_ms": md,
+                       "encode_gbs": fp16 / (me * 1e-3) / 1e9, "decode_gbs": fp16 / (md * 1e-3) / 1e9,
+                       "decode_frac_of_8TBs": (nb_ + fp16) / (md * 1e-3) / 1e9 / 8000.0}
+                      for s_, nb_, b_, me, md in zip(level_sets, nbytes_list, ebounds, ms_enc_sets, ms_dec_sets)],
         "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": peak, "unit": "GB/s", "frac": dec_ach / peak,
                      "traffic": traffic_for("k_decode", fp16), "kernel": "cg_decode",
                      "algorithmic_bytes_per_launch": dec_alg, "peak_kind": peak_kind,
@@ -661,7 +702,7 @@ def main():
         "decode_paged": paged,
         "decode_layer_groups": lgroups,
         "adaptive_streaming": adaptive,
-        "gpu_launches": args.steps * (3 + 6 + 2),
+        "gpu_launches": args.steps * (3 + nsets * (6 + 2)),
         "clocks": clk,
         "cpu_baseline": cpu,
         "setup": {"generate_s": gen_s},

@@ -318,6 +318,23 @@ cg_status cg_simulate_stream(int32_t n_chunks, int32_t n_levels, const uint64_t 
                              const cg_link_step *trace, int32_t n_steps, const uint8_t *levels,
                              const double *decode_s, double *timeline_out, double *total_s_out);
 
+/* The entropy bound of a container whose chunks are all coded at `level`
+ * with the tables of the last cg_fit_tables that used ws_fit_dev (whose
+ * histograms count exactly those symbols when the same KV is encoded):
+ * sum over the level's (layer, K/V, channel) tables of n_s log2(N / n_s)
+ * bits, / 8, plus 4 bytes per escape, plus the container's information-
+ * bearing structure (headers, chunk index, scales, anchors, stream offsets
+ * and stream headers, without padding).  It is the size an ideal coder of
+ * each table's empirical distribution would reach (Guide to CacheGen,
+ * pillar 3, "Distribution-Aware Arithmetic Coding"), the measure the
+ * container is held to within 1%.  The per-table terms are summed on the
+ * host in double (log2 evaluated in fp32 on the device).  Blocking: it reads
+ * the workspace after synchronising with the device.
+ * Errors: CG_ERR_INVALID_ARG (bad dims/params, level out of range, NULL),
+ * CG_ERR_CUDA. */
+cg_status cg_entropy_bound(const cg_dims *dims, const cg_params *params, const void *ws_fit_dev, int32_t level,
+                           double *bound_bytes);
+
 /* Status of the last call that used this workspace (blocking read of the
  * device status word; synchronise the call's stream first).  It reports the
  * device-side checks of the container format above (no passage of the pages

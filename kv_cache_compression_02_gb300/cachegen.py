@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "cg_decode": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                          P, P, S, P]),
             "cg_read_status": (ctypes.c_int, [P]),
+            "cg_entropy_bound": (ctypes.c_int, [D, Pr, P, ctypes.c_int32, ctypes.POINTER(ctypes.c_double)]),
             "cg_host_mapped": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_void_p)]),
             "cg_decode_noalloc": (ctypes.c_int, [D, Pr, P, P, ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
                                                  P, P, ctypes.POINTER(ctypes.c_void_p)]),
@@ -246,6 +247,15 @@ def cg_simulate_stream(chunk_bytes, trace, levels, decode_s):
     rc = lib().cg_simulate_stream(n, nl, cb.ctypes.data, ctypes.cast(arr, ctypes.c_void_p), ns, lv.ctypes.data,
                                   ds.ctypes.data, tl.ctypes.data, ctypes.byref(tot))
     return rc, tl, tot.value
+
+
+def cg_entropy_bound(cfg: Config, ws_fit, level: int = 0) -> float:
+    """Entropy bound (bytes) of a container with every chunk at `level`,
+    from the histograms of the last cg_fit_tables on ws_fit."""
+    out = ctypes.c_double(0.0)
+    check(lib().cg_entropy_bound(ctypes.byref(cfg.dims), ctypes.byref(cfg.params), _ptr(ws_fit), int(level),
+                                 ctypes.byref(out)), "cg_entropy_bound")
+    return out.value
 
 
 def cg_read_status(ws) -> int:

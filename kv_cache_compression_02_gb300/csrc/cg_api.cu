@@ -128,7 +128,9 @@ cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void
   float2 *scale = reinterpret_cast<float2 *>(ws + w.scale);
   if (e == cudaSuccess)
     e = launch_anchor_scales(lo, static_cast<const uint16_t *>(kv_dev), scale, nullptr, status, st);
-  if (e == cudaSuccess) e = launch_hist(lo, static_cast<const uint16_t *>(kv_dev), scale, tb, st);
+  if (e == cudaSuccess)
+    e = launch_hist(lo, static_cast<const uint16_t *>(kv_dev), scale, tb, reinterpret_cast<double *>(ws + w.ent_bits),
+                    reinterpret_cast<uint32_t *>(ws + w.ent_esc), st);
   return cuda_status(e);
 }
 
@@ -199,6 +201,38 @@ cg_status cg_decode_paged(const cg_dims *dims, const cg_params *params, const vo
   const PagedOut po{reinterpret_cast<uint16_t *const *>(pools_dev), block_table_dev, block_tokens, n_blocks};
   return decode_common(dims, params, tables_dev, bitstream_dev, bitstream_bytes, chunk_begin, chunk_end, 0, -1,
                        nullptr, &po, ws_dev, ws_bytes, stream);
+}
+
+cg_status cg_entropy_bound(const cg_dims *dims, const cg_params *params, const void *ws_fit_dev, int32_t level,
+                           double *bound_bytes) {
+  Layout lo;
+  if (!layout_of(dims, params, lo) || !ws_fit_dev || !bound_bytes || level < 0 || level >= lo.n_levels)
+    return CG_ERR_INVALID_ARG;
+  *bound_bytes = 0.0;
+  const FitWs w = fit_ws(lo);
+  const uint64_t per = uint64_t(lo.L) * 2 * lo.hd;  // tables of one level
+  std::vector<double> bits(per);
+  std::vector<uint32_t> esc(per);
+  const uint8_t *ws = static_cast<const uint8_t *>(ws_fit_dev);
+  if (cudaMemcpy(bits.data(), ws + w.ent_bits + 8 * uint64_t(level) * per, 8 * per, cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(esc.data(), ws + w.ent_esc + 4 * uint64_t(level) * per, 4 * per, cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return CG_ERR_CUDA;
+  double h = 0.0;
+  uint64_t n_esc = 0;
+  for (uint64_t t = 0; t < per; t++) {
+    h += bits[t];
+    n_esc += esc[t];
+  }
+  // structure that carries information: the header and chunk index; per chunk
+  // its header, scales, anchors and stream offsets; per stream its header
+  uint64_t fixed = 64 + 8 * uint64_t(lo.n_chunks);
+  for (int64_t k = 0; k < lo.n_chunks; k++)
+    fixed += 16 + 4 * uint64_t(lo.nstr) * lo.d + uint64_t(lo.nstr) * chunk_ng(lo, k) * lo.d + 4 * uint64_t(lo.nstr) +
+             16 * uint64_t(lo.nstr);
+  *bound_bytes = h / 8.0 + 4.0 * double(n_esc) + double(fixed);
+  return CG_OK;
 }
 
 cg_status cg_read_status(const void *ws_dev) {

@@ -317,12 +317,14 @@ k_anchor(Layout lo, const uint16_t *__restrict__ kv, float2 *__restrict__ scale_
 // takes one anchor group at a time: it rebuilds a_hat from the chunk's
 // scale, quantizes the group's deltas and counts the symbols into a shared
 // histogram of d rows of 257 counts.  Then one warp per channel normalises
-// its counts.
+// its counts and records, for the entropy bound of a container coded with
+// this level, the bits its symbols carry at their own frequencies,
+// sum_s n_s log2(N / n_s) (log2 in fp32, summed in fp64), and its escapes.
 constexpr int kHistThreads = 1024;
 
 __global__ void __launch_bounds__(kHistThreads)
 k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ scale,
-       uint8_t *__restrict__ tables) {
+       uint8_t *__restrict__ tables, double *__restrict__ ent_bits, uint32_t *__restrict__ ent_esc) {
   extern __shared__ __align__(16) uint32_t hist[];  // [d][257]
   const int lv = blockIdx.x, si = blockIdx.y;
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
@@ -437,6 +439,16 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
     uint64_t ix = tab_index(lo, lv, l, kvi, h * lo.d + c);
     *reinterpret_cast<uint4 *>(cdfv + ix * 256 + 8 * lane) =
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    double bits = 0.0;  // sum over the lane's symbols of n log2(N / n)
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+      if (n[i]) bits += double(n[i]) * double(log2f(float(N) / float(n[i])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
+    if (lane == 31) {  // lane 31 holds symbols 248..255: n[7] counts the escapes
+      ent_bits[ix] = bits;
+      ent_esc[ix] = n[7];
+    }
   }
 }
 
@@ -460,12 +472,12 @@ cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *s
 }
 
 cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
-                        uint8_t *tables, cudaStream_t st) {
+                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, cudaStream_t st) {
   const size_t smem = size_t(lo.d) * 257 * 4;
   cudaError_t e = cudaFuncSetAttribute(k_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, lo.nstr);
-  k_hist<<<grid, kHistThreads, smem, st>>>(lo, kv, scale, tables);
+  k_hist<<<grid, kHistThreads, smem, st>>>(lo, kv, scale, tables, ent_bits, ent_esc);
   return cudaGetLastError();
 }
 

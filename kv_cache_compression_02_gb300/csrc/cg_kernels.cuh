@@ -18,7 +18,7 @@ cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, 
 cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *scale_out,
                                  uint8_t *chunk_scratch, uint32_t *status, cudaStream_t st);
 cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
-                        uint8_t *tables, cudaStream_t st);
+                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, cudaStream_t st);
 
 // cg_encode.cu
 cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,

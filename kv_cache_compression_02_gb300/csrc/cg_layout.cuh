@@ -110,14 +110,17 @@ __host__ __device__ inline uint64_t words_per_symbol(const Layout &lo) { return 
 // ---- workspaces ----------------------------------------------------------
 // Every workspace starts with a 256-byte status block.
 struct FitWs {
-  uint64_t status, mult, scale, bytes;  // offsets
+  uint64_t status, mult, scale, ent_bits, ent_esc, bytes;  // offsets
 };
 inline FitWs fit_ws(const Layout &lo) {
   FitWs w;
+  const uint64_t nc = uint64_t(lo.n_levels) * lo.L * 2 * lo.hd;  // tables
   w.status = 0;
   w.mult = 256;                                                   // f32 [L][2]
   w.scale = pad256(w.mult + 8 * uint64_t(lo.L));                  // f32x2 [nk][nstr*d]
-  w.bytes = pad256(w.scale + 8 * uint64_t(lo.n_chunks) * lo.nstr * lo.d);
+  w.ent_bits = pad256(w.scale + 8 * uint64_t(lo.n_chunks) * lo.nstr * lo.d);  // f64 [tables]
+  w.ent_esc = pad256(w.ent_bits + 8 * nc);                        // u32 [tables]
+  w.bytes = pad256(w.ent_esc + 4 * nc);
   return w;
 }
 

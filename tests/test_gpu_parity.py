@@ -233,3 +233,36 @@ def test_special_values_bit_exact(orc, R, lb):
     st, y = gu.decode(cfg, tb_ref, cont_ref)
     assert rc == 0 and st == cg.CG_OK and np.array_equal(y, y_ref)
     assert (np.abs(y.view(np.float16).astype(np.float32)) <= 65504).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_workload", "d128_ragged_chunks", "d16_mixed_levels", "d64_escapes_R20",
+                                  "d32_kv_asymmetric", "d128_compact_escapes_R3"])
+def test_entropy_bound_matches_oracle(orc, name):
+    """cg_entropy_bound, from the fit's histograms, equals the oracle's
+    entropy bound of a container with every chunk at that level: sum of n_s
+    log2(N/n_s) per table / 8 + 4 bytes per escape + the structural bytes.
+    The per-table logarithms are fp32 on the device, so the two agree to a
+    few parts in 10^7."""
+    spec, C, G, R, lb, lm, _ = CASES[name]
+    x = synth.generate(spec)
+    cfg = cg.Config(spec.L, spec.H, spec.d, spec.S, C=C, G=G, R=R, level_base=lb, layer_mult=lm)
+    cd = orc.Codec(spec.L, spec.H, spec.d, spec.S, C=C, G=G, R=R)
+    kvd = gu.to_dev(x)
+    tb = cg.empty_u8(cg.cg_tables_bytes(cfg))
+    ws = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_FIT))
+    cg.check(cg.cg_fit_tables(cfg, kvd, tb, ws), "cg_fit_tables")
+    gu.torch().cuda.synchronize()
+    assert cg.cg_read_status(ws) == cg.CG_OK
+    rc, tb_ref = orc.fit_tables(cd, list(lb), lm, x)
+    assert rc == 0
+    for lv in range(len(lb)):
+        rc, cont, st = orc.encode(cd, len(lb), tb_ref, x, np.full(cd.n_chunks, lv, np.uint8))
+        assert rc == 0
+        want = orc.entropy_bound_bytes(st)
+        got = cg.cg_entropy_bound(cfg, ws, lv)
+        assert abs(got - want) <= 1e-6 * want, (lv, got, want)
+        assert cont.size >= got * (1 - 1e-6)  # no container beats the bound
+    if name == "d128_compact_escapes_R3":
+        assert st.n_esc > 0
+    with pytest.raises(cg.CacheGenError):
+        cg.cg_entropy_bound(cfg, ws, len(lb))
