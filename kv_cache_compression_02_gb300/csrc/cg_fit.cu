@@ -52,10 +52,11 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 // ---------------------------------------------------------------- k_stats
 // One CTA per head; each thread owns 4 channels and sums a strided subset of
 // the tokens.  An fp16 value is X = M * 2^E (times 2^-24) with M < 2^11 and
-// E <= 30, so X < 2^41; a 32-entry table gives 2^E and M's implicit bit for
-// each exponent field.  Most of the work is 32x32->64 multiply-adds, which
-// run on the FMA pipe beside the integer ALU:
-//   sum X    += (+-M) * 2^E                      (signed, 64-bit)
+// E <= 30, so X < 2^41; a 64-entry table gives 2^E and M's implicit bit for
+// each sign and exponent field (the sign carried by the signed 2^E, so the
+// signed sum needs no separate sign handling).  Most of the work is
+// 32x32->64 multiply-adds, which run on the FMA pipe beside the integer ALU:
+//   sum X    += M * (+-2^E)                      (signed, 64-bit)
 //   X = a 2^21 + b (a < 2^20, b < 2^21):
 //   sum X^2  = 2^42 sum a^2 + 2^21 sum 2ab + sum b^2
 // Each of the three partial sums takes terms below 2^42, so 2^18 tokens
@@ -68,12 +69,11 @@ struct Moments {
   uint64_t A2, AB, B2;
 };
 
-__device__ __forceinline__ void acc_moments(uint32_t h, const uint2 *ptab, Moments &m) {
-  const uint2 pe = ptab[(h >> 10) & 31u];  // (2^E, the implicit bit of M)
-  const uint32_t M = (h & 1023u) | pe.y;
-  const uint64_t X = uint64_t(M) * pe.x;
-  const int32_t sM = (h & 0x8000u) ? -int32_t(M) : int32_t(M);
-  m.T += int64_t(sM) * int32_t(pe.x);
+__device__ __forceinline__ void acc_moments(uint32_t h, const uint4 *ptab, Moments &m) {
+  const uint4 pe = ptab[h >> 10];  // (+-2^E with h's sign, 2^E, the implicit bit of M)
+  const uint32_t M = (h & 1023u) | pe.z;
+  const uint64_t X = uint64_t(M) * pe.y;
+  m.T += int64_t(int32_t(M)) * int32_t(pe.x);
   const uint32_t a = uint32_t(X >> 21), b = uint32_t(X) & 0x1FFFFFu;
   m.A2 += uint64_t(a) * a;
   m.AB += uint64_t(a) * (2u * b);
@@ -110,11 +110,11 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
         const float *__restrict__ mult, Bases bases, uint32_t *status) {
   extern __shared__ __align__(128) unsigned char smem[];  // kStatsStages tiles, then the reduction
   __shared__ __align__(8) uint64_t bars[kStatsStages];
-  __shared__ uint2 ptab[32];  // per exponent field e: (2^max(e-1, 0), e ? 1024 : 0)
+  __shared__ uint4 ptab[64];  // per sign and exponent field: (+-2^max(e-1, 0), 2^max(e-1, 0), e ? 1024 : 0)
   __shared__ int s_timeout;
-  if (threadIdx.x < 32) {
-    const uint32_t e = threadIdx.x;
-    ptab[e] = make_uint2(e ? 1u << (e - 1) : 1u, e ? 1024u : 0u);
+  if (threadIdx.x < 64) {
+    const uint32_t e = threadIdx.x & 31u, p = e ? 1u << (e - 1) : 1u;
+    ptab[threadIdx.x] = make_uint4(threadIdx.x & 32u ? uint32_t(-int32_t(p)) : p, p, e ? 1024u : 0u, 0u);
   }
   const int si = blockIdx.x;
   const int tpr = lo.d / 4;                 // threads per token row
