@@ -139,17 +139,17 @@ __device__ __forceinline__ int chan_of(int p) {
   return 4 * (r >> 1) + 2 * (p / (2 * T)) + (r & 1);
 }
 
-// The d cdf columns (global, [d][256] u16) -> cdfc rows 0..255, row 256
-// repeating cdf_255 (so that f_255, the escape, reads as 0) and a zero row
-// 257.  A thread takes 8 rows of one position (one 16-byte load);
-// neighbouring threads store neighbouring positions of a row.  A column
-// that does not start at 0 or does not strictly increase sets *bad.
-template <int T>
-__device__ __forceinline__ void build_cdf_columns(const uint16_t *cdf, uint16_t *cdfc, int *bad) {
-  constexpr int kRow = kLpt * T;
+// The d cdf columns (global, [d][256] u16) -> cdfc rows 0..255 (position p
+// of a row of kRow entries holding channel chan(p)), row 256 repeating
+// cdf_255 (so that f_255, the escape, reads as 0) and a zero row 257.  A
+// thread takes 8 rows of one position (one 16-byte load); neighbouring
+// threads store neighbouring positions of a row.  A column that does not
+// start at 0 or does not strictly increase sets *bad.
+template <int kRow, typename Chan>
+__device__ __forceinline__ void build_cdf_rows(const uint16_t *cdf, uint16_t *cdfc, int *bad, Chan chan) {
   for (int e = threadIdx.x; e < 32 * kRow; e += blockDim.x) {
     const int p = e % kRow, s0 = 8 * (e / kRow);
-    const uint16_t *src = cdf + chan_of<T>(p) * 256 + s0;
+    const uint16_t *src = cdf + chan(p) * 256 + s0;
     const uint4 v = *reinterpret_cast<const uint4 *>(src);
     const uint32_t nx = s0 + 8 < 256 ? uint32_t(src[8]) : kM;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -165,6 +165,13 @@ __device__ __forceinline__ void build_cdf_columns(const uint16_t *cdf, uint16_t 
     if (b) *bad = 1;
   }
   for (int p = threadIdx.x; p < kRow; p += blockDim.x) cdfc[257 * kRow + p] = 0;
+}
+
+// The same for the position order of k_decode's tables (thread i of a team
+// of T on lanes 4i..4i+3, bank i).
+template <int T>
+__device__ __forceinline__ void build_cdf_columns(const uint16_t *cdf, uint16_t *cdfc, int *bad) {
+  build_cdf_rows<kLpt * T>(cdf, cdfc, bad, [](int p) { return chan_of<T>(p); });
 }
 
 // First symbol of the neighbouring pair (sa, sa + 1) holding most of the
@@ -695,7 +702,8 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 // lane with state x the main entry's row is x & 0xFF00; a main entry of a
 // tail bucket is 0xFFFF, and the lane takes the fine entry at row
 // (x << 4) & 0xFF00 instead (bits 4..11 of the slot: rows 0..127 for the low
-// end, 128..255 for the high end).  The carry out of (x & 255) + entry gives
+// end, 128..255 for the high end); both entries are loaded and one selected,
+// which keeps the warp off a divergent branch.  The carry out of (x & 255) + entry gives
 // t with t & 0xFF00 = symbol * 256: the symbol's cdf row offset and, OR-ed
 // into the bits of 2^15, the exact fp32 2^15 + symbol.  A lane whose slot
 // still falls outside the pair (about 0.1% on the 70B-shaped workload), or
@@ -729,43 +737,62 @@ __device__ __forceinline__ uint32_t scan_step(uint32_t v) {
   return v;
 }
 
-// Pair entries for nb consecutive buckets of `width` slots (a power of two
-// up to 256) from slot `base`: entry b of column c is sa << 8 | (255 - the
-// last offset of sa's range in the bucket - bias), where (sa, sa + 1) is the
-// neighbouring pair holding most of the bucket.  For 16-slot buckets bias is
-// the bucket's offset in its 256-slot bucket (16 (b mod 16)), so that the
-// carry out of (x & 255) + entry is the same test as for the main table.
-// Buckets below flag_lo or from flag_hi get 0xFFFF instead.  A thread walks
-// 32 buckets of the two positions of one 32-bit word of the row, carrying
-// the current symbol from bucket to bucket.
-__device__ __forceinline__ void build_pairs(uint16_t *lut, const uint16_t *cdfc, int nb, uint32_t width,
-                                            uint32_t base, int flag_lo, int flag_hi) {
-  constexpr int kRowU = 128, kRun = 32;
-  for (int e = threadIdx.x; e < (nb / kRun) * 64; e += blockDim.x) {
-    const int wd = e % 64, b0 = kRun * (e / 64);
+// Bucket entries for the d = 128 tables (cdf rows of 128 u16 positions), one
+// thread per (bucket, position) with the position fastest, so that a warp's
+// threads read different banks, and four entries in flight per thread: the
+// symbol at the bucket's first slot by a binary search of the position's cdf
+// column, then the first symbol sa of the neighbouring pair holding most of
+// the bucket's `width` slots.  emit(b, p, sa, nxt, slot0) writes the entry
+// of bucket b (first slot slot0) at position p; nxt = cdf_(sa+1) (M for
+// sa = 255).
+template <typename Emit>
+__device__ __forceinline__ void build_buckets(const uint16_t *cdfc, int nb, uint32_t width, uint32_t base,
+                                              Emit emit) {
+  constexpr int kRowU = 128, kU = 4;
+  const int n = nb * kRowU;
+  for (int e0 = threadIdx.x; e0 < n; e0 += kU * int(blockDim.x)) {
+    uint32_t s[kU];  // largest s with cdf_s <= the bucket's first slot (cdf_0 = 0)
 #pragma unroll
-    for (int hpos = 0; hpos < 2; hpos++) {
-      const uint16_t *colp = cdfc + 2 * wd + hpos;
-      uint32_t s = 0;  // largest s with cdf_s <= the run's first slot (cdf_0 = 0)
+    for (int u = 0; u < kU; u++) s[u] = 0;
 #pragma unroll
-      for (uint32_t stp = 128; stp; stp >>= 1)
-        if (s + stp <= 255 && colp[(s + stp) * kRowU] <= base + width * b0) s += stp;
-      for (int bb = 0; bb < kRun; bb++) {
-        const int b = b0 + bb;
-        const uint32_t slot0 = base + width * b;
-        while (s < 255 && colp[(s + 1) * kRowU] <= slot0) s++;
-        uint16_t v = 0xFFFFu;
-        if (b >= flag_lo && b < flag_hi) {
-          const uint32_t sa = densest_pair<kRowU>(colp, s, slot0, width);
-          const uint32_t nxt = sa < 255 ? uint32_t(colp[(sa + 1) * kRowU]) : kM;
-          const uint32_t bnd = min(nxt - slot0, width) - 1;  // last offset of sa in the bucket
-          const uint32_t bias = width < 256 ? width * (uint32_t(b) & (256 / width - 1)) : 0u;
-          v = uint16_t((sa << 8) | (255 - bnd - bias));
-        }
-        lut[b * kRowU + 2 * wd + hpos] = v;
+    for (uint32_t stp = 128; stp; stp >>= 1) {
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+        const int e = min(e0 + u * int(blockDim.x), n - 1);  // (past the end: a repeat, never emitted)
+        const uint32_t slot0 = base + width * uint32_t(e / kRowU);
+        if (s[u] + stp <= 255 && cdfc[(s[u] + stp) * kRowU + e % kRowU] <= slot0) s[u] += stp;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; u++) {
+      const int e = e0 + u * int(blockDim.x);
+      if (e < n) {
+        const uint32_t p = e % kRowU, b = e / kRowU, slot0 = base + width * b;
+        const uint16_t *colp = cdfc + p;
+        const uint32_t sa = densest_pair<kRowU>(colp, s[u], slot0, width);
+        emit(b, p, sa, sa < 255 ? uint32_t(colp[(sa + 1) * kRowU]) : kM, slot0);
       }
     }
   }
+}
+
+// Pair entries for nb consecutive buckets of `width` slots (a power of two
+// up to 256) from slot `base`: entry b at position p is sa << 8 | (255 - the
+// last offset of sa's range in the bucket - bias).  For 16-slot buckets bias
+// is the bucket's offset in its 256-slot bucket (16 (b mod 16)), so that the
+// carry out of (x & 255) + entry is the same test as for the main table.
+// Buckets below flag_lo or from flag_hi get 0xFFFF instead.
+__device__ __forceinline__ void build_pairs(uint16_t *lut, const uint16_t *cdfc, int nb, uint32_t width,
+                                            uint32_t base, int flag_lo, int flag_hi) {
+  build_buckets(cdfc, nb, width, base, [&](uint32_t b, uint32_t p, uint32_t sa, uint32_t nxt, uint32_t slot0) {
+    uint16_t v = 0xFFFFu;
+    if (int(b) >= flag_lo && int(b) < flag_hi) {
+      const uint32_t bnd = min(nxt - slot0, width) - 1;  // last offset of sa in the bucket
+      const uint32_t bias = width < 256 ? width * (b & (256 / width - 1)) : 0u;
+      v = uint16_t((sa << 8) | (255 - bnd - bias));
+    }
+    lut[b * 128 + p] = v;
+  });
 }
 
 // Slow lane J (a slot outside the pair its bucket entry names, or the
@@ -938,7 +965,8 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   {                                                                                    \
     const uint32_t xx = x[J];                                                          \
     uint32_t lu = lds16(smb, kMainOff + colb<J>() + ((xx & 0xFF00u) | i4));            \
-    if (lu >= 0xFF00u) lu = lds16(smb, kFineOff + colb<J>() + (((xx << 4) & 0xFF00u) | i4)); \
+    const uint32_t lf = lds16(smb, kFineOff + colb<J>() + (((xx << 4) & 0xFF00u) | i4)); \
+    lu = lu >= 0xFF00u ? lf : lu;                                                      \
     const uint32_t t = (xx & 0xFFu) + lu;                                              \
     const uint32_t r = (t & 0xFF00u) | i4;                                    \
     const uint32_t c0 = lds16(smb, kCdfOff + colb<J>() + r);                  \
@@ -1023,14 +1051,19 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
               }
             }
           }
+          uint32_t nref = 0;
           if (pn > rbase + kHalf) {  // the first half is consumed: refill it with the next words
             __syncwarp();            // every thread's reads of it are done
             do {
               load_half(rbase + kRing);
               rbase += kHalf;
+              nref++;
             } while (pn > rbase + kHalf);
           }
-          lim = min(nw, rbase + kHalf);  // all but the refill just issued have landed
+          // all but the refill just issued have landed; after two refills
+          // (a token of more than kHalf words, possible only with many
+          // escapes) the first of them has not, and the next token waits
+          lim = min(nw, nref > 1 ? rbase : rbase + kHalf);
         } else {
           ring_words();
         }
@@ -1046,6 +1079,290 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     const bool lanes_ok = x[0] == kRansL && x[1] == kRansL && x[2] == kRansL && x[3] == kRansL;
     if (broken || !lanes_ok || p != nw || nesc != ne) atomicOr(status, kStCorrupt);
   }
+}
+
+// ---------------------------------------------------------------- thin ranges
+// The d = 128 decoder for chunk ranges that leave each (level, head) only a
+// chunk or two (a streamed chunk group of a mixed-level container).  With a
+// warp per stream such a CTA leaves its SM nearly idle, and a token costs
+// the warp's whole dependency chain (some 200 instructions).  Here a stream
+// is decoded by a team of four warps, one rANS lane per thread (lane 32 w + t
+// on thread t of the team's warp w), and a CTA holds two teams, one chunk
+// each.  Per token each warp finds its lanes' symbols and counts its words
+// with two ballots (renormalisation words, escapes); the four warp totals
+// meet in shared memory behind one named barrier of the team.  The tables
+// take 113 KB, so that two CTAs share an SM:
+//   main [240][128] u8  : for the 256-slot bucket (slot >> 8) - 8 of the
+//                         slots [2048, 63488), the first symbol sa (at most
+//                         254) of the neighbouring pair holding most of it;
+//   fine [128][128] u8  : the same for 32-slot buckets over [0, 2048) (rows
+//                         0..63) and [63488, 65536) (rows 64..127), the
+//                         distribution tails;
+//   cdf  [258][128] u16 : cdf_s of channel c at row s, position c (row 256
+//                         repeats cdf_255, row 257 is padding).
+// A lane loads cdf_sa, cdf_sa+1 and cdf_sa+2 and takes sa or sa + 1; a slot
+// outside the pair, or the escape (whose frequency then reads as 0), is
+// resolved by a binary search of the lane's cdf column.  A row holds the 128
+// channels in order, so a warp's 32 lanes read 32 consecutive entries of a
+// row: no bank conflicts.  Words are staged per team in a ring of two
+// halves that the team's first warp refills; a token whose words reach past
+// those known to have landed waits for them, behind one more barrier.
+constexpr int kThinTeams = 2;                                   // teams (streams) per CTA, 128 threads each
+constexpr uint32_t kThinTail = 2048;                            // slots with fine buckets, at each end
+constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 240
+constexpr uint32_t kThinFineRows = 2 * kThinTail / 32;          // 128
+constexpr uint32_t kThinFine = 0;
+constexpr uint32_t kThinMain = kThinFine + kThinFineRows * 128;
+constexpr uint32_t kThinCdf = kThinMain + kThinMainRows * 128;
+constexpr uint32_t kThinRing = kThinCdf + kCdfRows * 256;       // rings [teams][kRing] u16
+constexpr uint32_t kThinXch = kThinRing + kThinTeams * kRing * 2;  // word counts [teams][2][4] u32
+constexpr uint32_t kThinSmem = kThinXch + kThinTeams * 2 * 4 * 4;
+static_assert(kThinSmem + 64 + 1024 <= 233472 / 2, "two thin CTAs must share an SM");
+
+// First symbols of the densest neighbouring pairs, as u8 (at most 254), for
+// nb buckets of `width` slots from slot `base`, channel c at byte c of a
+// 128-byte row (the cdf rows hold channel c at position c).
+__device__ __forceinline__ void build_sa8(uint8_t *lut, const uint16_t *cdfr, int nb, uint32_t width,
+                                          uint32_t base) {
+  build_buckets(cdfr, nb, width, base, [&](uint32_t b, uint32_t p, uint32_t sa, uint32_t, uint32_t) {
+    lut[b * 128 + p] = uint8_t(min(sa, 254u));
+  });
+}
+
+__device__ __forceinline__ void team_bar(uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+template <bool PAGED>
+__global__ void __launch_bounds__(kThinTeams * 128, 2)
+k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
+          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
+  extern __shared__ __align__(16) uint8_t smb[];
+  __shared__ int s_bad;
+  __shared__ uint32_t s_nesc[kThinTeams];
+  uint16_t *cdfr = reinterpret_cast<uint16_t *>(smb + kThinCdf);
+
+  const int lv = blockIdx.x, si = blockIdx.y;
+  if (si < si_lo || si >= si_hi) return;  // outside the requested layers
+  const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
+  const int first = int(blockIdx.z) * kThinTeams;  // this CTA's entries of the level's chunk list
+  if (first >= cnt) return;
+  const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
+  uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+  const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
+
+  if (threadIdx.x < kThinTeams) s_nesc[threadIdx.x] = 0;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
+                        tab_index(lo, lv, l, kvi, h * lo.d) * 256;
+  build_cdf_rows<128>(cdf, cdfr, &s_bad, [](int p) { return p; });
+  __syncthreads();
+  build_sa8(smb + kThinMain, cdfr, kThinMainRows, 256, kThinTail);
+  build_sa8(smb + kThinFine, cdfr, kThinFineRows / 2, 32, 0);
+  build_sa8(smb + kThinFine + (kThinFineRows / 2) * 128, cdfr, kThinFineRows / 2, 32, kM - kThinTail);
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) atomicOr(status, kStCorrupt);
+    return;
+  }
+
+  // From here on the teams are independent: each syncs on its own barrier.
+  const int team = threadIdx.x >> 7;
+  const int idx = first + team;
+  if (idx >= cnt) return;  // a team without a chunk
+  const uint32_t ell = threadIdx.x & 127, wt = ell >> 5, lane = ell & 31, bar_id = 1 + team;
+  uint32_t ltm;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(ltm));
+  // the earlier warps' word counts, as masks on the exchanged counts
+  const uint32_t m1 = wt > 0 ? 0xFFFFu : 0u, m2 = wt > 1 ? 0xFFFFu : 0u, m3 = wt > 2 ? 0xFFFFu : 0u;
+  const float stp = reinterpret_cast<const float *>(tables + lo.tb_step)[tab_index(lo, lv, l, kvi, h * lo.d + ell)];
+  uint16_t *ring = reinterpret_cast<uint16_t *>(smb + kThinRing) + team * kRing;
+  uint32_t *xch = reinterpret_cast<uint32_t *>(smb + kThinXch) + team * 8;
+  // byte offsets of this lane's column in the main table (row 0 = the bucket
+  // of slot 0; rows below 8 and above 247 fall on the neighbouring tables
+  // and are never used), the fine table and the cdf rows
+  const uint32_t mcol = kThinMain - (kThinTail / 256) * 128 + ell, fcol = kThinFine + ell, ccol = kThinCdf + 2 * ell;
+
+  const int k = list[idx];
+  const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k), nd = chunk_nd(lo, k);
+  const uint64_t base = ld_u64(buf + 64 + 8 * uint64_t(k));
+  const uint64_t cend = (k + 1 < lo.n_chunks) ? ld_u64(buf + 64 + 8 * uint64_t(k + 1)) : ld_u64(buf + 48);
+  const uint8_t *chunk = buf + base;
+  const uint32_t *soffv = reinterpret_cast<const uint32_t *>(chunk + chunk_sec_off(lo, k));
+  const uint64_t so = soffv[si];
+  const uint64_t se = (si + 1 < lo.nstr) ? uint64_t(soffv[si + 1]) : (cend - base);
+  bool ok = !(so & 15) && so >= chunk_fixed(lo, k) && se >= so && base + se <= cend &&
+            se - so >= 16 + 4 * uint64_t(lo.d);
+  const uint8_t *blk = chunk + so;
+  uint32_t nw = 0, ne = 0;
+  if (ok) {
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    nw = hdr.x;
+    ne = hdr.y;
+    ok = hdr.z == uint32_t(nd) && hdr.w == 0 && 16 + 4 * uint64_t(lo.d) + 2 * uint64_t(nw) <= se - so;
+  }
+  if (!ok) {  // (the same for every thread of the team)
+    if (ell == 0) atomicOr(status, kStCorrupt);
+    return;
+  }
+  uint32_t x = reinterpret_cast<const uint32_t *>(blk + 16)[ell];
+  const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
+  const uint32_t wbytes = 2 * nw;
+  auto load_half = [&](uint32_t w0) {  // (first warp) words [w0, w0 + kHalf) -> ring half, zero past the end
+    const uint32_t b = 2 * w0 + 16 * lane;
+    const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
+    cp_async16(ring + ((w0 + 8 * lane) & (kRing - 1)), reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
+    cp_async_commit();
+  };
+  if (wt == 0) {
+    load_half(0);
+    load_half(kHalf);
+  }
+  // the ring holds words [rbase, rbase + kRing); words below lim (<= nw)
+  // are known to have landed.  All of these are the same across the team.
+  uint32_t rbase = 0, lim = 0, p = 0, par = 0, nesc = 0;
+  const float sc = reinterpret_cast<const float *>(chunk + lo.sec_s)[uint64_t(si) * lo.d + ell];
+  const int8_t *anc = reinterpret_cast<const int8_t *>(chunk + lo.sec_anc) + uint64_t(si) * ng * lo.d + ell;
+  bool broken = false;
+
+  // output row of the current token (this thread's lane in it)
+  uint16_t *orow;
+  bool row_ok = true, bad_row = false;
+  [[maybe_unused]] uint16_t *pool = nullptr;
+  [[maybe_unused]] int64_t lblk = 0, lblk_end = 0;
+  [[maybe_unused]] int left = 0;
+  [[maybe_unused]] int32_t bnext = 0;
+  if constexpr (PAGED) {
+    pool = po.pools[l * 2 + kvi];
+    const int64_t t0 = int64_t(k) * lo.C;
+    lblk = t0 / po.bt;
+    lblk_end = (t0 + ntok - 1) / po.bt + 1;
+    const int tib = int(t0 - lblk * po.bt);
+    left = po.bt - tib;
+    orow = paged_row(po, pool, po.table[lblk], tib, h, lo, 0, row_ok) + ell;
+    bad_row = !row_ok;
+    if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
+  } else {
+    orow = kv + (uint64_t(si) * lo.S + uint64_t(k) * lo.C) * lo.d + ell;
+  }
+  auto next_row = [&]() {
+    if constexpr (PAGED) {
+      if (--left == 0) {
+        left = po.bt;
+        if (++lblk < lblk_end) {
+          orow = paged_row(po, pool, bnext, 0, h, lo, 0, row_ok) + ell;
+          bad_row |= !row_ok;
+          if (lblk + 1 < lblk_end) bnext = po.table[lblk + 1];
+        }
+      } else {
+        orow += lo.d;
+      }
+    } else {
+      orow += lo.d;
+    }
+  };
+  auto store = [&](float v) {
+    if (!PAGED || row_ok) *orow = uint16_t(pack_f16x2(v, 0.0f) & 0xFFFFu);
+  };
+
+  int8_t an = anc[0];  // next group's anchor, loaded ahead
+  for (int g = 0; g < ng && !broken; g++) {
+    const float ah = __fmul_rn(float(an), sc);
+    if (g + 1 < ng) an = anc[uint64_t(g + 1) * lo.d];
+    store(ah);
+    next_row();
+    const int nt = min(lo.G, ntok - g * lo.G) - 1;  // delta tokens in this group
+    for (int tt = 0; tt < nt; tt++) {
+      // ---- symbol: the pair of the lane's bucket (fine at the tails)
+      const uint32_t slot = x & 0xFFFFu;
+      const uint32_t sm8 = smb[mcol + ((x >> 1) & 0x7F80u)];  // row slot >> 8
+      const uint32_t sf8 = smb[fcol + ((x << 2) & 0x3F80u)];  // row (slot >> 5) & 127: both tails
+      const uint32_t sa = ((slot + kThinTail) & 0xFFFFu) < 2 * kThinTail ? sf8 : sm8;
+      const uint32_t cb = ccol + sa * 256;
+      const uint32_t c0 = lds16(smb, cb), c1 = lds16(smb, cb + 256), c2 = lds16(smb, cb + 512);
+      const bool up = slot >= c1;
+      const uint32_t clo = up ? c1 : c0;
+      uint32_t f = (up ? c2 : c1) - clo, rr = slot - clo, s = sa + (up ? 1u : 0u);
+      uint32_t be = 0;  // lanes of the warp with an escape
+      if (__any_sync(0xffffffffu, rr >= f)) {
+        if (rr >= f) {  // outside the pair, or the escape: a binary search of the lane's column
+          uint32_t t = 0;  // largest t with cdf_t <= slot (cdf_0 = 0)
+#pragma unroll
+          for (uint32_t st = 128; st; st >>= 1)
+            if (lds16(smb, ccol + (t + st) * 256) <= slot) t += st;
+          const uint32_t a0 = lds16(smb, ccol + t * 256);
+          const uint32_t a1 = t < 255 ? lds16(smb, ccol + (t + 1) * 256) : kM;
+          f = a1 - a0;
+          rr = slot - a0;
+          s = t;
+        }
+        be = __ballot_sync(0xffffffffu, s == uint32_t(kEsc));
+      }
+      x = f * (x >> 16) + rr;
+      const bool ndw = x < kRansL;
+      // ---- word positions: lane order within the warp, warp order within
+      // the team; an escape's raw value takes two more words
+      const uint32_t bn = __ballot_sync(0xffffffffu, ndw);
+      xch[par * 4 + wt] = (__popc(bn) + 2 * __popc(be)) | (be ? 0x10000u : 0u);
+      team_bar(bar_id);
+      const uint4 xv = *reinterpret_cast<const uint4 *>(xch + par * 4);
+      par ^= 1;
+      const uint32_t sum = xv.x + xv.y + xv.z + xv.w;
+      const uint32_t pn = p + (sum & 0xFFFFu);
+      const uint32_t pos = p + (xv.x & m1) + (xv.y & m2) + (xv.z & m3) + __popc(bn & ltm) + 2 * __popc(be & ltm);
+      float v;
+      if (pn > lim || sum > 0xFFFFu) {  // (the same across the team)
+        // ---- rare token: its words reach past those known to have landed
+        // (or past the stream's end), or an escape's raw value is among them
+        if (pn > nw) {
+          broken = true;
+          break;
+        }
+        if (wt == 0) cp_async_wait_all();  // every word issued so far has landed ...
+        team_bar(bar_id);                  // ... and is visible to the team
+        if (sum <= 0xFFFFu) {
+          const uint32_t w = ring[pos & (kRing - 1)];
+          if (ndw) x = __byte_perm(w, x, 0x5410);  // x<<16 | w
+          v = __fmaf_rn(__int_as_float(0x4B400000 + int(s)) - 12583039.0f, stp, ah);
+        } else {  // escapes: the raw q follows the lane's renormalisation word; read from the container
+          const uint32_t q0 = pos + (ndw ? 1u : 0u);
+          if (ndw) x = __byte_perm(uint32_t(words[pos]), x, 0x5410);
+          if (s == uint32_t(kEsc)) {
+            const int q = int(uint32_t(words[q0]) | (uint32_t(words[q0 + 1]) << 16));
+            nesc++;
+            v = __fmaf_rn(__int2float_rn(q), stp, ah);
+          } else {
+            v = __fmaf_rn(__int_as_float(0x4B400000 + int(s)) - 12583039.0f, stp, ah);
+          }
+        }
+        uint32_t nref = 0;
+        if (pn > rbase + kHalf) {  // the first half is consumed: refill it with the next words
+          team_bar(bar_id);        // every lane's reads of it are done
+          do {
+            if (wt == 0) load_half(rbase + kRing);
+            rbase += kHalf;
+            nref++;
+          } while (pn > rbase + kHalf);
+        }
+        // all but the refill just issued have landed (after two, the next token waits)
+        lim = min(nw, nref > 1 ? rbase : rbase + kHalf);
+      } else {
+        const uint32_t w = ring[pos & (kRing - 1)];
+        if (ndw) x = __byte_perm(w, x, 0x5410);  // x<<16 | w
+        // q = s - 127 as an exact fp32: (1.5*2^23 + s) - (1.5*2^23 + 127)
+        v = __fmaf_rn(__int_as_float(0x4B400000 + int(s)) - 12583039.0f, stp, ah);
+      }
+      p = pn;
+      store(v);
+      next_row();
+    }
+  }
+  if (wt == 0) cp_async_wait_all();  // no copy may land after the CTA has gone
+  if (PAGED && bad_row) atomicOr(status, kStBadArg);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) nesc += __shfl_xor_sync(0xffffffffu, nesc, o);
+  if (lane == 0 && nesc) atomicAdd(&s_nesc[team], nesc);
+  team_bar(bar_id);
+  if (x != kRansL || (ell == 0 && (broken || p != nw || s_nesc[team] != ne))) atomicOr(status, kStCorrupt);
 }
 
 template <int T, bool PAGED, bool COMPACT>
@@ -1081,6 +1398,22 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
   return cudaGetLastError();
 }
 
+// Thin ranges: a CTA per (level, head, pair of the level's chunks); CTAs
+// past the level's chunk count return at once.
+template <bool PAGED>
+cudaError_t launch_decode_thin(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
+                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+  cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kThinSmem));
+  if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
+    e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kThinTeams - 1) / kThinTeams);
+  k_thin128<PAGED><<<grid, kThinTeams * 128, kThinSmem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
+                                                              l1 * 2 * lo.H);
+  return cudaGetLastError();
+}
+
 // chunks: the chunks in the range.  A CTA decodes one (level, head), one
 // team per chunk of that level.  When a CTA can be expected to hold at
 // most 12 chunks (a range of at most 12, or several levels sharing the
@@ -1095,11 +1428,15 @@ cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint
                              int l0, int l1) {
   constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
   const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
-  if (T == 32 && (chunks <= 12 || 2 * per_level <= 12)) {
-    const int teams = chunks <= 12 ? (chunks < 8 ? 8 : chunks) : 12;
-    return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+  if constexpr (T == 32) {
+    if (per_level <= kThinTeams)
+      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
+    if (chunks <= 12 || 2 * per_level <= 12) {
+      const int teams = chunks <= 12 ? (chunks < 8 ? 8 : chunks) : 12;
+      return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
+    }
+    return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
   }
-  if constexpr (T == 32) return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
   const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
   return launch_decode_tpb<T, PAGED, false>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
 }

@@ -75,3 +75,27 @@ def test_empty_and_invalid_layer_ranges(case):
     assert cg.cg_decode_layers(cfg, tbd, cd_, cont.size, 0, -1, 2, 2, kv, ws) == cg.CG_OK  # nothing to do
     T.cuda.synchronize()
     assert (kv.cpu().numpy().view(np.uint16) == FILL).all()
+
+
+def test_layer_groups_d128_thin_range(orc):
+    """Layer groups of a short chunk range at d = 128 (the thin-range
+    decoder): each group's tokens equal the oracle's, the rest is untouched."""
+    spec = synth.GenSpec(L=3, H=1, d=128, S=600, seed=52, innov="t3", rho=(0.85, 0.99), n_outliers=1,
+                         outlier_scale=20.0)
+    C, G, lb = 128, 10, (0.05, 0.2)
+    x = synth.generate(spec)
+    cd = orc.Codec(spec.L, spec.H, spec.d, spec.S, C=C, G=G)
+    cfg = cg.Config(spec.L, spec.H, spec.d, spec.S, C, G=G, level_base=lb)
+    levels = np.array([1, 0, 0, 1, 1], np.uint8)
+    rc, tb = orc.fit_tables(cd, list(lb), None, x)
+    assert rc == 0
+    rc, cont, _ = orc.encode(cd, len(lb), tb, x, levels)
+    assert rc == 0
+    rc, y_ref = orc.decode(tb, cont, 1, 4)
+    assert rc == 0
+    sts, y = _decode_groups(cfg, spec, tb, cont, [(1, 2), (2, 3)], k0=1, k1=4)
+    assert sts == [cg.CG_OK] * 2
+    t0, t1 = 1 * C, 4 * C
+    assert np.array_equal(y[1:, :, :, t0:t1], y_ref[1:, :, :, t0:t1])
+    assert (y[0] == FILL).all()
+    assert (y[:, :, :, :t0] == FILL).all() and (y[:, :, :, t1:] == FILL).all()

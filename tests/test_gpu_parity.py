@@ -53,6 +53,15 @@ CASES = {
                           np.array([[0.25, 1.0], [0.5, 2.0], [1.0, 4.0]], np.float32), None),
     "d128_compact_escapes_R3": (synth.GenSpec(L=1, H=1, d=128, S=300, seed=31, innov="t3", rho=(0.85, 0.9)),
                                 100, 10, 3, (0.05,), None, None),
+    # d = 128 with at most two chunks per (level, head): the thin-range
+    # decoder (a team of four warps per stream); R = 3 makes escapes common,
+    # so tokens whose words outrun the staging ring come up too
+    "d128_thin_escapes_R3": (synth.GenSpec(L=1, H=2, d=128, S=200, seed=33, innov="t3", rho=(0.85, 0.9)),
+                             100, 10, 3, (0.05,), None, None),
+    # eight chunks over four levels, two each; the last chunk is ragged
+    "d128_thin_mixed_ragged": (synth.GenSpec(L=2, H=2, d=128, S=1000, seed=34, innov="t3", rho=(0.85, 0.99),
+                                             n_outliers=2, outlier_scale=20.0), 128, 10, 127,
+                               (0.05, 0.1, 0.2, 0.4), None, [0, 1, 2, 3, 3, 2, 1, 0]),
 }
 
 
@@ -104,6 +113,22 @@ def test_chunk_range_decode(orc):
         assert (y[:, :, :, :t0] == 0x1234).all() and (y[:, :, :, t1:] == 0x1234).all()
 
 
+def test_chunk_range_decode_d128(orc):
+    """Small chunk ranges at d = 128 (the thin-range decoder, and the
+    compact one for three chunks of a level): each equals the oracle's
+    decode of that range, and no other token is written."""
+    x, cd, cfg, levels, lb, lm = _setup(orc, "d128_thin_mixed_ragged")
+    rc, tb = orc.fit_tables(cd, list(lb), lm, x)
+    rc, cont, _ = orc.encode(cd, len(lb), tb, x, levels)
+    _, full = orc.decode(tb, cont)
+    for k0, k1 in ((0, 1), (1, 3), (5, 8), (7, 8), (0, 8), (2, 2)):
+        st, y = gu.decode(cfg, tb, cont, k0, k1, fill=0x1234)
+        assert st == cg.CG_OK
+        t0, t1 = k0 * cd.C, min(k1 * cd.C, cd.S)
+        assert np.array_equal(y[:, :, :, t0:t1], full[:, :, :, t0:t1]), (k0, k1)
+        assert (y[:, :, :, :t0] == 0x1234).all() and (y[:, :, :, t1:] == 0x1234).all()
+
+
 def test_gpu_roundtrip_error_bound(orc):
     """GPU fit -> GPU encode -> GPU decode on a Llama-3-70B-like slice."""
     w = W.scaled(W.LLAMA3_70B, L=2, S=4608)
@@ -131,8 +156,9 @@ def _small(orc, name="d8_group7"):
     return x, cd, cfg, levels, tb, cont
 
 
-# d = 8; d = 128 with 3 chunks (compact tables); d = 128 with 42 chunks (full tables)
-@pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams"])
+# d = 8; d = 128 with 3 chunks (compact tables); d = 128 with 42 chunks (full
+# tables); d = 128 with two chunks per level (thin-range decoder)
+@pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams", "d128_thin_mixed_ragged"])
 def test_corrupt_containers_flagged(orc, name):
     x, cd, cfg, levels, tb, cont = _small(orc, name)
     assert gu.decode(cfg, tb, cont)[0] == cg.CG_OK
