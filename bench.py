@@ -56,6 +56,9 @@ def parse():
                     help="skip the layer-group, paged-cache and adaptive-streaming legs")
     ap.add_argument("--layers", type=int, default=0,
                     help="run the same workload with fewer layers (a smaller case for profiling)")
+    ap.add_argument("--stream-groups", type=int, default=0,
+                    help="also decode the container group by group of this many chunks on a side stream, "
+                         "each group as soon as its bytes have been copied from pinned host memory")
     return ap.parse_args()
 
 
@@ -517,6 +520,60 @@ def main():
                 ts.append(a.elapsed_time(b))
         link[name] = nb_ / (statistics.mean(ts) * 1e-3) / 1e9
 
+    # chunk-group streaming: group g's container bytes are copied from pinned
+    # host memory on one stream, and the group decodes on another as soon as
+    # they have landed, while group g + 1 is being copied; against the copy
+    # alone and the one-shot decode from device memory
+    streamed = None
+    if args.stream_groups:
+        G = args.stream_groups
+        copy_s, dec_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        win = [(lo_, lo_ + (1 << 22)) for lo_ in (0, kv.numel() // 2, kv.numel() - (1 << 22))]
+        ref = [kv_out[a_:b_].clone() for a_, b_ in win]  # kv_out holds the serial end-to-end decode
+
+        def timed(fn, s0, s1):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s0)
+            fn()
+            b.record(s1)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+
+        def stream_groups():
+            for g0 in range(0, w.n_chunks, G):
+                g1 = min(g0 + G, w.n_chunks)
+                lo_b = 0 if g0 == 0 else offs[g0]  # the first group carries the header and chunk index
+                with torch.cuda.stream(copy_s):
+                    cont_dev[lo_b:offs[g1]].copy_(cont_host[lo_b:offs[g1]], non_blocking=True)
+                arrived = torch.cuda.Event()
+                arrived.record(copy_s)
+                dec_s.wait_event(arrived)
+                cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, g0, g1, kv_out, ws_dec, dec_s), "cg_decode")
+
+        def copy_alone():
+            with torch.cuda.stream(copy_s):
+                cont_dev.copy_(cont_host, non_blocking=True)
+
+        def decode_alone():
+            cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, 0, -1, kv_out, ws_dec, dec_s), "cg_decode")
+
+        kv_out.zero_()
+        t_stream = [timed(stream_groups, copy_s, dec_s) for _ in range(3)]
+        cg.check(cg.cg_read_status(ws_dec), "decode (streamed)")
+        for (a_, b_), r_ in zip(win, ref):
+            if not torch.equal(kv_out[a_:b_], r_):
+                raise RuntimeError("streamed decode differs from the one-shot decode")
+        t_copy = min(timed(copy_alone, copy_s, copy_s) for _ in range(3))
+        t_dec = min(timed(decode_alone, dec_s, dec_s) for _ in range(3))
+        t_s = min(t_stream)
+        streamed = {"groups_of_chunks": G, "ms": t_s, "copy_ms": t_copy, "decode_ms": t_dec,
+                    "overlap_efficiency": max(t_copy, t_dec) / t_s, "fp16_gbs": w.fp16_bytes / (t_s * 1e-3) / 1e9,
+                    "what": "container copied group by group from pinned host memory on one stream, each group "
+                            "decoded on another once its bytes have landed; efficiency = max(copy alone, one-shot "
+                            "decode) / streamed"}
+        del ref
+
     # the same decode in layer groups, in execution order: 19 layers (304
     # CTAs, two full waves) per launch, an event after each group
     lgroups = None
@@ -701,6 +758,7 @@ def main():
                            "what": "container H2D, one cg_decode, KV D2H, in sequence"}},
         "decode_paged": paged,
         "decode_layer_groups": lgroups,
+        "decode_streamed": streamed,
         "adaptive_streaming": adaptive,
         "gpu_launches": args.steps * (3 + nsets * (6 + 2)),
         "clocks": clk,

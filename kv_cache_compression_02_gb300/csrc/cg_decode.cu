@@ -3,22 +3,27 @@
 // CacheGen's receiver decodes the bitstream "in real time, synchronized
 // with transmission" (gptget summary of arXiv 2310.07240, Methodology; Guide
 // to CacheGen, pillar 4) and rebuilds each token as anchor + delta (Guide,
-// Step 2 decode_sequence; Step 1 dequantize).  Two kernels:
+// Step 2 decode_sequence; Step 1 dequantize).  The kernels:
 //
 //   k_decode_index  one thread checks the container header against the
 //                   caller's dims and the tables header, validates the
 //                   chunk index and headers of [k0, k1) and lists the chunks
 //                   of each level.
-//   k_decode        one CTA per (level, head) holds that head's d frequency
-//                   tables in shared memory, laid out so that thread i of a
-//                   team only ever touches bank i (no bank conflicts however
-//                   the symbols fall); each team of d/4 threads decodes one
-//                   chunk's stream, 4 rANS lanes per thread.  Per token: a
-//                   bucket lookup (slot >> 7) plus one carry finds the
-//                   symbol, a shuffle scan over the team orders the word
-//                   reads, the fused dequantisation fma(q, step, a_hat) is
-//                   clamped, converted to fp16 and stored 8 bytes per thread
-//                   (a team writes one 256-byte token row).
+//   k_decode        (d < 128) one CTA per (level, head) holds that head's d
+//                   frequency tables in shared memory, laid out so that
+//                   thread i of a team only ever touches bank i (no bank
+//                   conflicts however the symbols fall); each team of d/4
+//                   threads decodes one chunk's stream, 4 rANS lanes per
+//                   thread.  Per token: a bucket lookup (slot >> 7) plus one
+//                   carry finds the symbol, a shuffle scan over the team
+//                   orders the word reads, the fused dequantisation
+//                   fma(q, step, a_hat) is clamped, converted to fp16 and
+//                   stored 8 bytes per thread (a team writes one token row).
+//   k_dec128        (d = 128) the same with a warp per chunk stream and
+//                   tables laid out for a short token loop.
+//   k_thin128       (d = 128, chunk ranges that give each (level, head) only
+//                   a few chunks) four warps per stream, one lane per
+//                   thread, for a short dependency chain per token.
 //
 // Every read of the container is bounded by the stream's own header, which
 // is itself checked against the stream index; a stream whose lanes do not
@@ -61,14 +66,9 @@ __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wa
 // a copy of its first kMirror words, so that a thread's (up to four) words
 // can be read from one base index without wrapping.
 constexpr uint32_t kRing = 512, kHalf = 256, kMirror = 16;
-// (compact tables read word by word and keep no mirror)
-template <bool COMPACT>
-__host__ __device__ constexpr uint32_t ring_stride() { return COMPACT ? kRing : kRing + kMirror; }
 // Symbol-search buckets: slot >> kBucketShift, kBuckets of them.
 constexpr uint32_t kBucketShift = 7, kBuckets = 1u << (16 - kBucketShift), kBucketSlots = 1u << kBucketShift;
 constexpr uint32_t kCdfRows = 258;  // cdf_0 .. cdf_255, cdf_255 again, padding
-// Compact tables (two CTAs per SM): one u8 entry per 256-slot bucket.
-constexpr uint32_t kCBuckets = 256, kCBucketSlots = 256;
 
 // ---------------------------------------------------------------- index
 __global__ void k_decode_index(Layout lo, const uint8_t *__restrict__ tables,
@@ -224,30 +224,8 @@ __device__ __forceinline__ void build_lut16(uint16_t *lut16, const uint16_t *cdf
   }
 }
 
-// Compact bucket entries: lut8 [256 buckets][4 lanes x T] u8 = sa of each
-// 256-slot bucket (at most 254), thread i's four lanes in word i.
-template <int T>
-__device__ __forceinline__ void build_lut8(uint8_t *lut8, const uint16_t *cdfc) {
-  constexpr int kRow = kLpt * T;
-  for (int e = threadIdx.x; e < 4 * kRow; e += blockDim.x) {
-    const int c = e % kRow, b0 = 64 * (e / kRow);
-    const int ti = c >> 2, j = c & 3;
-    const uint16_t *colp = cdfc + (j >> 1) * 2 * T + 2 * ti + (j & 1);
-    uint32_t s = 0;
-#pragma unroll
-    for (uint32_t stp = 128; stp; stp >>= 1)
-      if (s + stp <= 255 && colp[(s + stp) * kRow] <= kCBucketSlots * b0) s += stp;
-    for (int bb = 0; bb < 64; bb++) {
-      const uint32_t slot0 = kCBucketSlots * (b0 + bb);
-      while (s < 255 && colp[(s + 1) * kRow] <= slot0) s++;
-      const uint32_t sa = densest_pair<kRow>(colp, s, slot0, kCBucketSlots);
-      lut8[(b0 + bb) * kRow + c] = uint8_t(min(sa, 254u));
-    }
-  }
-}
-
 // ---------------------------------------------------------------- decode
-// Shared memory per CTA (d lanes, T = d/4 threads per team), 215 KB at d=128
+// Shared memory per CTA (d lanes, T = d/4 threads per team), 119 KB at d = 64
 // with 22 teams:
 //   lut16 [512 buckets][4 lanes x T] u16 : sa << 8 | (255 - last offset of sa
 //                                          in the 128-slot bucket), where
@@ -256,31 +234,18 @@ __device__ __forceinline__ void build_lut8(uint8_t *lut8, const uint16_t *cdfc) 
 //   cdfc  [258 rows][4 lanes x T] u16    : cdf_s for s < 256; row 256 repeats
 //                                          cdf_255; row 257 is padding
 //   rings [teams][512 + 16] u16          : the staged words of each team
-//                                          (512 with the compact tables)
 // Thread i of a team owns lanes 4i..4i+3; within a row its two 32-bit words
 // (lanes 0-1 and 2-3) sit at word index i and T + i, so with T = 32 every
 // access of thread i to lut16 or cdfc hits bank i, whatever the symbols.
 // PAGED: token rows go to the paged cache po instead of kv.
-// COMPACT: for launches whose CTAs have few chunks (small chunk ranges,
-// mixed-level containers), tables small enough for two CTAs per SM: the
-// bucket table is lut8 [256 buckets][4 lanes x T] u8 holding only sa (the
-// densest pair's first symbol, at most 254) of each 256-slot bucket, in
-// lane order (thread i's four entries are word i: bank i); the search
-// loads cdf_sa, cdf_sa+1 and cdf_sa+2 and picks sa or sa + 1.  Such CTAs
-// also take word positions from one ballot per bit of the word counts
-// instead of a shuffle scan: more instructions, a shorter dependency chain,
-// which pays when few warps share the SM.
-template <int T, bool PAGED, bool COMPACT>
+template <int T, bool PAGED>
 __global__ void __launch_bounds__(max_threads<T>())
 k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
-  constexpr bool BALLOT = COMPACT;
   extern __shared__ __align__(16) uint32_t smem[];
-  uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);            // [kBuckets][2][T][2]
-  uint8_t *lut8 = reinterpret_cast<uint8_t *>(smem);               // COMPACT: [kCBuckets][T][4]
-  uint16_t *cdfc = COMPACT ? reinterpret_cast<uint16_t *>(lut8 + kCBuckets * kLpt * T)
-                           : lut16 + kBuckets * kLpt * T;              // [kCdfRows][2][T][2]
-  uint16_t *rings = cdfc + kCdfRows * kLpt * T;                      // [teams][ring_stride] words
+  uint16_t *lut16 = reinterpret_cast<uint16_t *>(smem);  // [kBuckets][2][T][2]
+  uint16_t *cdfc = lut16 + kBuckets * kLpt * T;          // [kCdfRows][2][T][2]
+  uint16_t *rings = cdfc + kCdfRows * kLpt * T;          // [teams][kRing + kMirror] words
   __shared__ int s_bad;
 
   const int lv = blockIdx.x, si = blockIdx.y;
@@ -296,11 +261,9 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   __syncthreads();
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
                         tab_index(lo, lv, l, kvi, h * lo.d) * 256;
-  constexpr int kRow = kLpt * T;  // u16 entries per table row
   build_cdf_columns<T>(cdf, cdfc, &s_bad);
   __syncthreads();
-  if constexpr (COMPACT) build_lut8<T>(lut8, cdfc);
-  else build_lut16<T>(lut16, cdfc);
+  build_lut16<T>(lut16, cdfc);
   __syncthreads();
   if (s_bad) {
     if (threadIdx.x == 0) atomicOr(status, kStCorrupt);
@@ -309,15 +272,12 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 
   const int team = threadIdx.x / T, i = threadIdx.x % T, nteams = blockDim.x / T;
   const uint32_t tm = team_mask<T>();
-  [[maybe_unused]] uint32_t ltm = 0;  // lanes below this one
-  if constexpr (BALLOT) asm("mov.u32 %0, %%lanemask_lt;" : "=r"(ltm));
   const float4 st4 = *reinterpret_cast<const float4 *>(
       reinterpret_cast<const float *>(tables + lo.tb_step) + tab_index(lo, lv, l, kvi, h * lo.d + kLpt * i));
   const float step[4] = {st4.x, st4.y, st4.z, st4.w};
   // thread i's entries: u16 index row * (4T) + (j>>1)*2T + 2i + (j&1); with
   // T = 32 a row is 256 bytes, so the bucket row of state x is x & 0xFF00.
   const uint16_t *lt = lut16 + 2 * i;
-  [[maybe_unused]] const uint8_t *lt8 = lut8 + kLpt * i;  // COMPACT: lane j of thread i at lt8[b * 4T + j]
   const uint16_t *ct = cdfc + 2 * i;
 
   for (int idx = team; idx < cnt; idx += nteams) {
@@ -350,7 +310,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     uint32_t x[4] = {xs.x, xs.y, xs.z, xs.w};
     const uint16_t *__restrict__ words = reinterpret_cast<const uint16_t *>(blk + 16 + 4 * lo.d);
     // stage the first kRing words (two halves) of the stream in the ring
-    uint16_t *ring = rings + team * ring_stride<COMPACT>();
+    uint16_t *ring = rings + team * (kRing + kMirror);
     const uint32_t wbytes = 2 * nw;
     auto load_half = [&](uint32_t w0) {  // words [w0, w0 + kHalf) -> ring half
       for (uint32_t o = 16 * i; o < 2 * kHalf; o += 16 * T) {
@@ -358,7 +318,7 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
         cp_async16(ring + ((w0 + o / 2) & (kRing - 1)), reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
       }
-      if (!COMPACT && (w0 & (kRing - 1)) == 0 && 16 * uint32_t(i) < 2 * kMirror) {  // the mirror of ring[0, kMirror)
+      if ((w0 & (kRing - 1)) == 0 && 16 * uint32_t(i) < 2 * kMirror) {  // the mirror of ring[0, kMirror)
         const uint32_t b = 2 * w0 + 16 * i;
         const uint32_t n = b < wbytes ? min(16u, wbytes - b) : 0u;
         cp_async16(ring + kRing + 8 * i, reinterpret_cast<const uint8_t *>(words) + (n ? b : 0), n);
@@ -435,72 +395,21 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 #pragma unroll
         for (int j = 0; j < 4; j++) {
           const int cj = (j >> 1) * T * 2 + (j & 1);
-          if constexpr (COMPACT) {
-            const uint32_t slot = x[j] & 0xFFFFu;
-            const uint32_t sa = lt8[(slot >> 8) * (kLpt * T) + j];
-            const uint32_t c0 = ct[sa * (kLpt * T) + cj];
-            const uint32_t c1 = ct[(sa + 1) * (kLpt * T) + cj];
-            const uint32_t c2 = ct[(sa + 2) * (kLpt * T) + cj];
-            const bool up = slot >= c1;
-            const uint32_t clo = up ? c1 : c0;
-            ff[j] = (up ? c2 : c1) - clo;
-            rr[j] = slot - clo;  // wraps above 0xFFFF when the slot is below sa
-            sy[j] = sa + (up ? 1u : 0u);
-          } else {
-            const uint32_t b = (x[j] >> kBucketShift) & (kBuckets - 1);
-            const uint32_t lu = lt[b * (kLpt * T) + cj];
-            // carry out of the low byte adds one when the slot is past s0's part of the bucket
-            const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
-            const uint32_t c0 = ct[sj * (kLpt * T) + cj];
-            const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
-            ff[j] = c1 - c0;
-            rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
-            sy[j] = sj;
-          }
+          const uint32_t b = (x[j] >> kBucketShift) & (kBuckets - 1);
+          const uint32_t lu = lt[b * (kLpt * T) + cj];
+          // carry out of the low byte adds one when the slot is past s0's part of the bucket
+          const uint32_t sj = ((x[j] & (kBucketSlots - 1)) + lu) >> 8;
+          const uint32_t c0 = ct[sj * (kLpt * T) + cj];
+          const uint32_t c1 = ct[(sj + 1) * (kLpt * T) + cj];
+          ff[j] = c1 - c0;
+          rr[j] = (x[j] & 0xFFFFu) - c0;  // wraps above 0xFFFF when the slot is below sa
+          sy[j] = sj;
           sl[j] = rr[j] >= ff[j];
         }
-        // Slow lanes: about 1% of lanes (more with the compact tables' wider
-        // buckets).  Symbol 255 is the escape, whose raw value follows in the
-        // words.
+        // Slow lanes: about 1% of lanes.  Symbol 255 is the escape, whose
+        // raw value follows in the words.
         uint32_t escm = 0;
-        if constexpr (T == 32 && COMPACT) {
-          // Compact tables: the whole warp resolves a slow lane at a time.
-          // The owner's slot goes to every thread; thread r reads row 8r of
-          // the owner's cdf column, and since the rows increase, one ballot
-          // counts the rows at or below the slot and so fixes its group of
-          // 8 symbols; a second ballot over the group's rows (and the next
-          // row, for the frequency) gives the symbol.  No thread diverges.
-          // (With the full tables' narrower buckets, most slow lanes sit one
-          // or two symbols from the pair and the per-lane binary search below
-          // is cheaper.)
-          if (__any_sync(0xffffffffu, sl[0] | sl[1] | sl[2] | sl[3])) {
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-              const int cj = (j >> 1) * T * 2 + (j & 1);
-              const uint32_t slot = x[j] & 0xFFFFu;
-              for (uint32_t m = __ballot_sync(0xffffffffu, sl[j]); m; m &= m - 1) {
-                const int t = __ffs(m) - 1;
-                const uint32_t st = __shfl_sync(0xffffffffu, slot, t);
-                const int col = 2 * t + cj;  // the owner's column within a cdf row
-                const uint32_t cr8 = cdfc[(8 * uint32_t(i)) * kRow + col];
-                const uint32_t g = 8 * (__popc(__ballot_sync(0xffffffffu, cr8 <= st)) - 1);  // cdf_0 = 0
-                const uint32_t r = g + uint32_t(i);
-                const bool win = i < 9 && r <= 255u;
-                const uint32_t crow = cdfc[(win ? r : g) * kRow + col];
-                const uint32_t c = __popc(__ballot_sync(0xffffffffu, win && i < 8 && crow <= st));  // >= 1
-                const uint32_t s = g + c - 1;
-                const uint32_t c0 = __shfl_sync(0xffffffffu, crow, (c - 1) & 31);
-                const uint32_t c1 = __shfl_sync(0xffffffffu, crow, c & 31);
-                if (i == t) {
-                  sy[j] = s;
-                  ff[j] = (s < 255 ? c1 : kM) - c0;
-                  rr[j] = st - c0;
-                  escm |= s == uint32_t(kEsc) ? (1u << j) : 0u;
-                }
-              }
-            }
-          }
-        } else if (sl[0] | sl[1] | sl[2] | sl[3]) {
+        if (sl[0] | sl[1] | sl[2] | sl[3]) {
           // a binary search in the lane's own table column, between the
           // previous bucket's pair and the chosen pair when the slot is below
           // it, else between the pair and the next bucket's pair
@@ -510,32 +419,18 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
               const int cj = (j >> 1) * T * 2 + (j & 1);
               const uint32_t slot = x[j] & 0xFFFFu;
               uint32_t lo = sy[j], hi = lo;
-              if constexpr (COMPACT) {
-                // the neighbours' sa bound the symbol (sa + 1 above: sa stops at 254)
-                const uint32_t b = slot >> 8;
-                if (rr[j] > 0xFFFFu) {
-                  hi = lo - 1;
-                  lo = b > 0 ? uint32_t(lt8[(b - 1) * (kLpt * T) + j]) : 0u;
-                } else if (lo < 255) {
-                  lo += 1;
-                  hi = b + 1 < kCBuckets ? uint32_t(lt8[(b + 1) * (kLpt * T) + j]) + 1u : 255u;
-                }
-              } else {
-                const uint32_t b = slot >> kBucketShift;
-                if (rr[j] > 0xFFFFu) {  // below the pair: down to the previous bucket's pair
-                  hi = lo - 1;
-                  lo = b > 0 ? (lt[(b - 1) * (kLpt * T) + cj] >> 8) : 0u;
-                } else if (lo < 255) {  // above the pair (255: the escape symbol, already found)
-                  lo += 1;  // cdf_lo <= slot is known
-                  hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
-                }
+              const uint32_t b = slot >> kBucketShift;
+              if (rr[j] > 0xFFFFu) {  // below the pair: down to the previous bucket's pair
+                hi = lo - 1;
+                lo = b > 0 ? (lt[(b - 1) * (kLpt * T) + cj] >> 8) : 0u;
+              } else if (lo < 255) {  // above the pair (255: the escape symbol, already found)
+                lo += 1;  // cdf_lo <= slot is known
+                hi = b + 1 < kBuckets ? (lt[(b + 1) * (kLpt * T) + cj] >> 8) : 255u;
               }
-              {
-                while (lo < hi) {
-                  const uint32_t mid = (lo + hi + 1) >> 1;
-                  if (ct[mid * (kLpt * T) + cj] <= slot) lo = mid;
-                  else hi = mid - 1;
-                }
+              while (lo < hi) {
+                const uint32_t mid = (lo + hi + 1) >> 1;
+                if (ct[mid * (kLpt * T) + cj] <= slot) lo = mid;
+                else hi = mid - 1;
               }
               const uint32_t c0 = ct[lo * (kLpt * T) + cj];
               const uint32_t c1 = lo < 255 ? uint32_t(ct[(lo + 1) * (kLpt * T) + cj]) : kM;
@@ -554,22 +449,14 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         }
         const int cntw = int(nd4[0]) + int(nd4[1]) + int(nd4[2]) + int(nd4[3]) + 2 * __popc(escm);  // 0..12 words
         // ---- word positions: team-wide exclusive scan of the word counts
-        uint32_t tot, excl;
-        if constexpr (BALLOT) {
-          const uint32_t b0 = __ballot_sync(tm, cntw & 1) & tm, b1 = __ballot_sync(tm, cntw & 2) & tm;
-          const uint32_t b2 = __ballot_sync(tm, cntw & 4) & tm, b3 = __ballot_sync(tm, cntw & 8) & tm;
-          tot = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2) + 8 * __popc(b3);
-          excl = __popc(b0 & ltm) + 2 * __popc(b1 & ltm) + 4 * __popc(b2 & ltm) + 8 * __popc(b3 & ltm);
-        } else {
-          int incl = cntw;
+        int incl = cntw;
 #pragma unroll
-          for (int o = 1; o < T; o <<= 1) {
-            const int v = __shfl_up_sync(tm, incl, o, T);
-            if (i >= o) incl += v;
-          }
-          tot = uint32_t(__shfl_sync(tm, incl, T - 1, T));
-          excl = uint32_t(incl - cntw);
+        for (int o = 1; o < T; o <<= 1) {
+          const int v = __shfl_up_sync(tm, incl, o, T);
+          if (i >= o) incl += v;
         }
+        const uint32_t tot = uint32_t(__shfl_sync(tm, incl, T - 1, T));
+        const uint32_t excl = uint32_t(incl - cntw);
         uint32_t pos = p + excl;
         bool in_ring = true;
         if (p + tot > lim) {  // past the words known to be staged, or a refill may be due
@@ -602,34 +489,20 @@ k_decode(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
         float v[4];
         if (in_ring) {
         if (escm == 0) {
-          if constexpr (COMPACT) {  // thin launches: per-lane reads (the shorter dependency chain pays)
+          // the thread's words are consecutive from pos: read four (the
+          // mirror covers reads past the ring's end; unneeded ones are
+          // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
+          const uint16_t *rp = ring + (pos & (kRing - 1));
+          const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3];
+          const uint32_t a1 = nd4[0] ? w1 : w0, a2 = nd4[0] ? w2 : w1, a3 = nd4[0] ? w3 : w2;
+          const uint32_t b2 = nd4[1] ? a2 : a1, b3 = nd4[1] ? a3 : a2;
+          const uint32_t wl[4] = {w0, a1, b2, nd4[2] ? b3 : b2};
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-              {
-                const uint32_t w = ring[pos & (kRing - 1)];  // read unconditionally, use if needed
-                const bool nd = nd4[j];
-                x[j] = nd ? __byte_perm(w, x[j], 0x5410) : x[j];  // x<<16 | w
-                pos += nd ? 1u : 0u;
-              }
-              // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
-              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
-              v[j] = __fmaf_rn(qf, step[j], ah[j]);
-            }
-          } else {
-            // the thread's words are consecutive from pos: read four (the
-            // mirror covers reads past the ring's end; unneeded ones are
-            // ignored) and give lane j word number nd_0 + .. + nd_(j-1)
-            const uint16_t *rp = ring + (pos & (kRing - 1));
-            const uint32_t w0 = rp[0], w1 = rp[1], w2 = rp[2], w3 = rp[3];
-            const uint32_t a1 = nd4[0] ? w1 : w0, a2 = nd4[0] ? w2 : w1, a3 = nd4[0] ? w3 : w2;
-            const uint32_t b2 = nd4[1] ? a2 : a1, b3 = nd4[1] ? a3 : a2;
-            const uint32_t wl[4] = {w0, a1, b2, nd4[2] ? b3 : b2};
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-              x[j] = nd4[j] ? __byte_perm(wl[j], x[j], 0x5410) : x[j];  // x<<16 | w
-              const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;  // as above
-              v[j] = __fmaf_rn(qf, step[j], ah[j]);
-            }
+          for (int j = 0; j < 4; j++) {
+            x[j] = nd4[j] ? __byte_perm(wl[j], x[j], 0x5410) : x[j];  // x<<16 | w
+            // q = sy - 127 as an exact fp32 (|q| < 2^22): (1.5*2^23 + sy) - (1.5*2^23 + 127)
+            const float qf = __int_as_float(0x4B400000 + int(sy[j])) - 12583039.0f;
+            v[j] = __fmaf_rn(qf, step[j], ah[j]);
           }
         } else {  // escapes: the raw q follows the lane's renormalisation word
 #pragma unroll
@@ -1102,59 +975,66 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 //                         repeats cdf_255, row 257 is padding).
 // A lane loads cdf_sa, cdf_sa+1 and cdf_sa+2 and takes sa or sa + 1; a slot
 // outside the pair, or the escape (whose frequency then reads as 0), is
-// resolved by a binary search of the lane's cdf column.  A row holds the 128
-// channels in order, so a warp's 32 lanes read 32 consecutive entries of a
-// row: no bank conflicts.  Words are staged per team in a ring of two
+// resolved by a binary search of the lane's cdf column.  The rows are laid
+// out so that lane 32 w + t (thread t of the team's warp w) only ever
+// touches bank t, whatever rows its warp reads: its u8 entries are byte
+// 4 t + w of a row, its cdf entries u16 position 2 t + 64 (w >> 1) + (w & 1)
+// (byte 4 t + 128 (w >> 1) + 2 (w & 1)).  Words are staged per team in a ring of two
 // halves that the team's first warp refills; a token whose words reach past
 // those known to have landed waits for them, behind one more barrier.
-constexpr int kThinTeams = 2;                                   // teams (streams) per CTA, 128 threads each
+constexpr int kThinTeamsMax = 8;                                // teams (streams) per CTA, 128 threads each
 constexpr uint32_t kThinTail = 2048;                            // slots with fine buckets, at each end
 constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 240
 constexpr uint32_t kThinFineRows = 2 * kThinTail / 32;          // 128
 constexpr uint32_t kThinFine = 0;
 constexpr uint32_t kThinMain = kThinFine + kThinFineRows * 128;
 constexpr uint32_t kThinCdf = kThinMain + kThinMainRows * 128;
-constexpr uint32_t kThinRing = kThinCdf + kCdfRows * 256;       // rings [teams][kRing] u16
-constexpr uint32_t kThinXch = kThinRing + kThinTeams * kRing * 2;  // word counts [teams][2][4] u32
-constexpr uint32_t kThinSmem = kThinXch + kThinTeams * 2 * 4 * 4;
-static_assert(kThinSmem + 64 + 1024 <= 233472 / 2, "two thin CTAs must share an SM");
+constexpr uint32_t kThinRing = kThinCdf + kCdfRows * 256;  // rings [teams][kRing] u16, then word counts [teams][2][4] u32
+__host__ __device__ constexpr uint32_t thin_smem(int teams) { return kThinRing + uint32_t(teams) * (kRing * 2 + 32); }
+static_assert(thin_smem(2) + 64 + 1024 <= 233472 / 2, "two 2-team thin CTAs must share an SM");
+
+// The thin tables' column of lane 32 w + t: u16 position p = 2 t + 64 (w >> 1)
+// + (w & 1) of a cdf row, and the lane and u8 byte of position p.
+__device__ __forceinline__ int thin_lane(int p) { return 32 * (((p >> 6) << 1) | (p & 1)) + ((p >> 1) & 31); }
+__device__ __forceinline__ uint32_t thin_byte(uint32_t p) { return 4 * ((p >> 1) & 31) + (((p >> 6) << 1) | (p & 1)); }
 
 // First symbols of the densest neighbouring pairs, as u8 (at most 254), for
-// nb buckets of `width` slots from slot `base`, channel c at byte c of a
-// 128-byte row (the cdf rows hold channel c at position c).
+// nb buckets of `width` slots from slot `base`, at each lane's byte of a
+// 128-byte row.
 __device__ __forceinline__ void build_sa8(uint8_t *lut, const uint16_t *cdfr, int nb, uint32_t width,
                                           uint32_t base) {
   build_buckets(cdfr, nb, width, base, [&](uint32_t b, uint32_t p, uint32_t sa, uint32_t, uint32_t) {
-    lut[b * 128 + p] = uint8_t(min(sa, 254u));
+    lut[b * 128 + thin_byte(p)] = uint8_t(min(sa, 254u));
   });
 }
 
 __device__ __forceinline__ void team_bar(uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
 template <bool PAGED>
-__global__ void __launch_bounds__(kThinTeams * 128, 2)
+__global__ void __launch_bounds__(kThinTeamsMax * 128)
 k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
           uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
-  __shared__ uint32_t s_nesc[kThinTeams];
+  __shared__ uint32_t s_nesc[kThinTeamsMax];
   uint16_t *cdfr = reinterpret_cast<uint16_t *>(smb + kThinCdf);
+  const int nteams = int(blockDim.x >> 7);
 
   const int lv = blockIdx.x, si = blockIdx.y;
   if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
-  const int first = int(blockIdx.z) * kThinTeams;  // this CTA's entries of the level's chunk list
+  const int first = int(blockIdx.z) * nteams;  // this CTA's entries of the level's chunk list
   if (first >= cnt) return;
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
 
-  if (threadIdx.x < kThinTeams) s_nesc[threadIdx.x] = 0;
+  if (threadIdx.x < kThinTeamsMax) s_nesc[threadIdx.x] = 0;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
                         tab_index(lo, lv, l, kvi, h * lo.d) * 256;
-  build_cdf_rows<128>(cdf, cdfr, &s_bad, [](int p) { return p; });
+  build_cdf_rows<128>(cdf, cdfr, &s_bad, [](int p) { return thin_lane(p); });
   __syncthreads();
   build_sa8(smb + kThinMain, cdfr, kThinMainRows, 256, kThinTail);
   build_sa8(smb + kThinFine, cdfr, kThinFineRows / 2, 32, 0);
@@ -1176,11 +1056,12 @@ k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restri
   const uint32_t m1 = wt > 0 ? 0xFFFFu : 0u, m2 = wt > 1 ? 0xFFFFu : 0u, m3 = wt > 2 ? 0xFFFFu : 0u;
   const float stp = reinterpret_cast<const float *>(tables + lo.tb_step)[tab_index(lo, lv, l, kvi, h * lo.d + ell)];
   uint16_t *ring = reinterpret_cast<uint16_t *>(smb + kThinRing) + team * kRing;
-  uint32_t *xch = reinterpret_cast<uint32_t *>(smb + kThinXch) + team * 8;
+  uint32_t *xch = reinterpret_cast<uint32_t *>(smb + kThinRing + nteams * kRing * 2) + team * 8;
   // byte offsets of this lane's column in the main table (row 0 = the bucket
   // of slot 0; rows below 8 and above 247 fall on the neighbouring tables
-  // and are never used), the fine table and the cdf rows
-  const uint32_t mcol = kThinMain - (kThinTail / 256) * 128 + ell, fcol = kThinFine + ell, ccol = kThinCdf + 2 * ell;
+  // and are never used), the fine table and the cdf rows: bank `lane`
+  const uint32_t mcol = kThinMain - (kThinTail / 256) * 128 + 4 * lane + wt, fcol = kThinFine + 4 * lane + wt,
+                 ccol = kThinCdf + 4 * lane + 128 * (wt >> 1) + 2 * (wt & 1);
 
   const int k = list[idx];
   const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k), nd = chunk_nd(lo, k);
@@ -1365,20 +1246,14 @@ k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restri
   if (x != kRansL || (ell == 0 && (broken || p != nw || s_nesc[team] != ne))) atomicOr(status, kStCorrupt);
 }
 
-template <int T, bool PAGED, bool COMPACT>
+template <int T, bool PAGED>
 cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
                               uint8_t *ws, int teams, cudaStream_t st, const PagedOut &po, int l0, int l1) {
-  const size_t tabs = COMPACT ? size_t(kCBuckets) * lo.d + size_t(kCdfRows) * lo.d * 2
-                              : size_t(kBuckets + kCdfRows) * lo.d * 2;
-  const size_t smem = tabs + size_t(teams) * ring_stride<COMPACT>() * 2;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_decode<T, PAGED, COMPACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two compact CTAs fit
-    e = cudaFuncSetAttribute(k_decode<T, PAGED, COMPACT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             int(cudaSharedmemCarveoutMaxShared));
+  const size_t smem = size_t(kBuckets + kCdfRows) * lo.d * 2 + size_t(teams) * (kRing + kMirror) * 2;
+  cudaError_t e = cudaFuncSetAttribute(k_decode<T, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
-  k_decode<T, PAGED, COMPACT>
+  k_decode<T, PAGED>
       <<<grid, teams * T, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
 }
@@ -1398,47 +1273,48 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
   return cudaGetLastError();
 }
 
-// Thin ranges: a CTA per (level, head, pair of the level's chunks); CTAs
-// past the level's chunk count return at once.
+// Thin ranges: a CTA per (level, head, `teams` of the level's chunks); CTAs
+// past the level's chunk count return at once.  Two teams: two CTAs share
+// an SM; eight: one CTA holds eight streams of a level on the SM's one table.
 template <bool PAGED>
 cudaError_t launch_decode_thin(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
-                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
-  cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kThinSmem));
+                               uint8_t *ws, int chunks, int teams, cudaStream_t st, const PagedOut &po, int l0,
+                               int l1) {
+  const int smem = int(thin_smem(teams));
+  cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(thin_smem(kThinTeamsMax)));
   if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
     e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              int(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kThinTeams - 1) / kThinTeams);
-  k_thin128<PAGED><<<grid, kThinTeams * 128, kThinSmem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
-                                                              l1 * 2 * lo.H);
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + teams - 1) / teams);
+  k_thin128<PAGED><<<grid, teams * 128, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
   return cudaGetLastError();
 }
 
-// chunks: the chunks in the range.  A CTA decodes one (level, head), one
-// team per chunk of that level.  When a CTA can be expected to hold at
-// most 12 chunks (a range of at most 12, or several levels sharing the
-// range thinly: twice the mean per level at most 12), the compact tables
-// let two CTAs share an SM, with 8 to 12 teams each (a team takes a second
-// chunk if its level has more).  Otherwise a CTA has one team per chunk,
-// and at least 512 threads so that the table build is spread wide; teams
-// without a chunk only build.
+// chunks: the chunks in the range.  d = 128: when the levels share the
+// range thinly (a mean of at most two chunks per level), the thin-range
+// kernel with two teams per CTA, two CTAs per SM; with at most eight per
+// level in a range of at most 16 chunks, the thin-range kernel with eight
+// teams per CTA; otherwise k_dec128, a warp per chunk.  Other d: k_decode,
+// a team per chunk of the CTA's level, and at least 512 threads so that the
+// table build is spread wide (teams without a chunk only build).
 template <int T, bool PAGED>
 cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint8_t *buf,
                              uint16_t *kv, uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po,
                              int l0, int l1) {
-  constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
-  const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
   if constexpr (T == 32) {
-    if (per_level <= kThinTeams)
-      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
-    if (chunks <= 12 || 2 * per_level <= 12) {
-      const int teams = chunks <= 12 ? (chunks < 8 ? 8 : chunks) : 12;
-      return launch_decode_tpb<T, PAGED, true>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
-    }
+    const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
+    if (per_level <= 2)
+      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, 2, st, po, l0, l1);
+    if (per_level <= 8 && chunks <= 16)
+      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, 8, st, po, l0, l1);
     return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
+  } else {
+    constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
+    const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
+    return launch_decode_tpb<T, PAGED>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
   }
-  const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
-  return launch_decode_tpb<T, PAGED, false>(lo, tables, buf, kv, ws, teams, st, po, l0, l1);
 }
 
 template <int T>

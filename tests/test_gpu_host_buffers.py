@@ -3,8 +3,9 @@ output KV in pinned host memory mapped into the device address space, so
 the decoder reads the words and writes the tokens across the host link
 (the receiver decodes a streamed context as it arrives: Guide to CacheGen,
 pillar 4).  Every result must equal the oracle's decode, bit for bit, with
-both decoder table layouts (a full-table launch for 15 chunks, a compact
-one for a 3-chunk range)."""
+each d = 128 decoder (a warp per stream for 15 chunks; the thin-range
+kernel for a 3-chunk range with eight teams per CTA and for a 2-chunk range
+with two)."""
 import numpy as np
 import pytest
 
@@ -65,13 +66,15 @@ def test_full_decode_host_to_host(orc, case):
     assert np.array_equal(_run(case, 0, -1), want)
 
 
-def test_chunk_range_host_to_host_writes_only_its_tokens(orc, case):
+@pytest.mark.parametrize("k0,k1", [(4, 7), (13, 15)])
+def test_chunk_range_host_to_host_writes_only_its_tokens(orc, case, k0, k1):
     spec, cfg, tb, cont = case
-    rc, ref = orc.decode(tb, cont, 4, 7)
+    rc, ref = orc.decode(tb, cont, k0, k1)
     assert rc == 0
+    t0, t1 = k0 * 128, min(k1 * 128, spec.S)
     want = np.full_like(ref, FILL)
-    want[..., 4 * 128:7 * 128, :] = ref[..., 4 * 128:7 * 128, :]
-    assert np.array_equal(_run(case, 4, 7), want)
+    want[..., t0:t1, :] = ref[..., t0:t1, :]
+    assert np.array_equal(_run(case, k0, k1), want)
 
 
 def test_mapped_address_only_for_page_locked_host_memory(case):

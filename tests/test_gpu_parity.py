@@ -42,16 +42,15 @@ CASES = {
                                  (0.1,), None, None),
     "many_chunks_teams": (synth.GenSpec(L=1, H=1, d=128, S=2100, seed=29, innov="t3", rho=(0.85, 0.99)),
                           50, 10, 127, (0.1, 0.3), None, [i % 2 for i in range(42)]),
-    # d = 128 with few chunks per (level, head): the compact-table decoder;
-    # here one level holds 21 of 24 chunks, more than a CTA's 12 teams
-    "d128_compact_second_round": (synth.GenSpec(L=1, H=2, d=128, S=960, seed=30, innov="t3", rho=(0.85, 0.99),
+    # d = 128, 24 chunks of four levels, one level holding 21 of them
+    "d128_levels_uneven": (synth.GenSpec(L=1, H=2, d=128, S=960, seed=30, innov="t3", rho=(0.85, 0.99),
                                                 n_outliers=2, outlier_scale=20.0), 40, 10, 127,
                                   (0.05, 0.1, 0.2, 0.4), None, [0] * 21 + [1, 2, 3]),
     # separate K and V multipliers per layer (finer steps for keys)
     "d32_kv_asymmetric": (synth.GenSpec(L=3, H=2, d=32, S=400, seed=32, innov="t3", rho=(0.85, 0.99), n_outliers=1,
                                         outlier_scale=20.0), 128, 10, 127, (0.1,),
                           np.array([[0.25, 1.0], [0.5, 2.0], [1.0, 4.0]], np.float32), None),
-    "d128_compact_escapes_R3": (synth.GenSpec(L=1, H=1, d=128, S=300, seed=31, innov="t3", rho=(0.85, 0.9)),
+    "d128_three_chunks_escapes_R3": (synth.GenSpec(L=1, H=1, d=128, S=300, seed=31, innov="t3", rho=(0.85, 0.9)),
                                 100, 10, 3, (0.05,), None, None),
     # d = 128 with at most two chunks per (level, head): the thin-range
     # decoder (a team of four warps per stream); R = 3 makes escapes common,
@@ -114,9 +113,9 @@ def test_chunk_range_decode(orc):
 
 
 def test_chunk_range_decode_d128(orc):
-    """Small chunk ranges at d = 128 (the thin-range decoder, and the
-    compact one for three chunks of a level): each equals the oracle's
-    decode of that range, and no other token is written."""
+    """Small chunk ranges at d = 128 (the thin-range decoder, with two and
+    with eight teams per CTA): each equals the oracle's decode of that range,
+    and no other token is written."""
     x, cd, cfg, levels, lb, lm = _setup(orc, "d128_thin_mixed_ragged")
     rc, tb = orc.fit_tables(cd, list(lb), lm, x)
     rc, cont, _ = orc.encode(cd, len(lb), tb, x, levels)
@@ -156,8 +155,9 @@ def _small(orc, name="d8_group7"):
     return x, cd, cfg, levels, tb, cont
 
 
-# d = 8; d = 128 with 3 chunks (compact tables); d = 128 with 42 chunks (full
-# tables); d = 128 with two chunks per level (thin-range decoder)
+# d = 8; d = 128 with 3 chunks (thin-range decoder, eight teams); d = 128 with
+# 42 chunks (a warp per stream); d = 128 with two chunks per level (thin-range
+# decoder, two teams)
 @pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams", "d128_thin_mixed_ragged"])
 def test_corrupt_containers_flagged(orc, name):
     x, cd, cfg, levels, tb, cont = _small(orc, name)
@@ -262,7 +262,7 @@ def test_special_values_bit_exact(orc, R, lb):
 
 
 @pytest.mark.parametrize("name", ["tiny_workload", "d128_ragged_chunks", "d16_mixed_levels", "d64_escapes_R20",
-                                  "d32_kv_asymmetric", "d128_compact_escapes_R3"])
+                                  "d32_kv_asymmetric", "d128_three_chunks_escapes_R3"])
 def test_entropy_bound_matches_oracle(orc, name):
     """cg_entropy_bound, from the fit's histograms, equals the oracle's
     entropy bound of a container with every chunk at that level: sum of n_s
@@ -288,7 +288,7 @@ def test_entropy_bound_matches_oracle(orc, name):
         got = cg.cg_entropy_bound(cfg, ws, lv)
         assert abs(got - want) <= 1e-6 * want, (lv, got, want)
         assert cont.size >= got * (1 - 1e-6)  # no container beats the bound
-    if name == "d128_compact_escapes_R3":
+    if name == "d128_three_chunks_escapes_R3":
         assert st.n_esc > 0
     with pytest.raises(cg.CacheGenError):
         cg.cg_entropy_bound(cfg, ws, len(lb))
