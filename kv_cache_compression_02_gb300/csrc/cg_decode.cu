@@ -960,19 +960,20 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 // warp per stream such a CTA leaves its SM nearly idle, and a token costs
 // the warp's whole dependency chain (some 200 instructions).  Here a stream
 // is decoded by a team of four warps, one rANS lane per thread (lane 32 w + t
-// on thread t of the team's warp w), and a CTA holds two teams, one chunk
+// on thread t of the team's warp w), and a CTA holds four teams, one chunk
 // each.  Per token each warp finds its lanes' symbols and counts its words
-// with two ballots (renormalisation words, escapes); the four warp totals
-// meet in shared memory behind one named barrier of the team.  The tables
-// take 113 KB, so that two CTAs share an SM:
-//   main [240][128] u8  : for the 256-slot bucket (slot >> 8) - 8 of the
-//                         slots [2048, 63488), the first symbol sa (at most
-//                         254) of the neighbouring pair holding most of it;
-//   fine [128][128] u8  : the same for 32-slot buckets over [0, 2048) (rows
-//                         0..63) and [63488, 65536) (rows 64..127), the
-//                         distribution tails;
-//   cdf  [258][128] u16 : cdf_s of channel c at row s, position c (row 256
-//                         repeats cdf_255, row 257 is padding).
+// with a ballot (and one for escapes when a lane of the warp took the
+// search); the four warp totals meet in shared memory behind one named
+// barrier of the team.  The tables take 104 KB, so that two CTAs (eight
+// streams, the most that the registers allow) share an SM:
+//   fine [64][128] u8   : for 32-slot buckets over [0, 1024) (rows 0..31) and
+//                         [64512, 65536) (rows 32..63), the distribution
+//                         tails, the first symbol sa (at most 254) of the
+//                         neighbouring pair holding most of the bucket;
+//   main [248][128] u8  : the same for the 256-slot bucket (slot >> 8) - 4
+//                         of the slots [1024, 64512);
+//   cdf  [258][128] u16 : cdf_s of lane 32 w + t at row s (row 256 repeats
+//                         cdf_255, row 257 is padding).
 // A lane loads cdf_sa, cdf_sa+1 and cdf_sa+2 and takes sa or sa + 1; a slot
 // outside the pair, or the escape (whose frequency then reads as 0), is
 // resolved by a binary search of the lane's cdf column.  The rows are laid
@@ -982,16 +983,17 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 // (byte 4 t + 128 (w >> 1) + 2 (w & 1)).  Words are staged per team in a ring of two
 // halves that the team's first warp refills; a token whose words reach past
 // those known to have landed waits for them, behind one more barrier.
-constexpr int kThinTeamsMax = 8;                                // teams (streams) per CTA, 128 threads each
-constexpr uint32_t kThinTail = 2048;                            // slots with fine buckets, at each end
-constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 240
-constexpr uint32_t kThinFineRows = 2 * kThinTail / 32;          // 128
+constexpr int kThinTeams = 4;                                   // teams (streams) per CTA, 128 threads each
+constexpr int kThinPerLevel = 6;                                // thin launches: mean chunks per level at most this
+constexpr uint32_t kThinTail = 1024;                            // slots with fine buckets, at each end
+constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 248
+constexpr uint32_t kThinFineRows = 2 * kThinTail / 32;          // 64
 constexpr uint32_t kThinFine = 0;
 constexpr uint32_t kThinMain = kThinFine + kThinFineRows * 128;
 constexpr uint32_t kThinCdf = kThinMain + kThinMainRows * 128;
 constexpr uint32_t kThinRing = kThinCdf + kCdfRows * 256;  // rings [teams][kRing] u16, then word counts [teams][2][4] u32
 __host__ __device__ constexpr uint32_t thin_smem(int teams) { return kThinRing + uint32_t(teams) * (kRing * 2 + 32); }
-static_assert(thin_smem(2) + 64 + 1024 <= 233472 / 2, "two 2-team thin CTAs must share an SM");
+static_assert(thin_smem(kThinTeams) + 64 + 1024 <= 233472 / 2, "two thin CTAs must share an SM");
 
 // The thin tables' column of lane 32 w + t: u16 position p = 2 t + 64 (w >> 1)
 // + (w & 1) of a cdf row, and the lane and u8 byte of position p.
@@ -1011,12 +1013,12 @@ __device__ __forceinline__ void build_sa8(uint8_t *lut, const uint16_t *cdfr, in
 __device__ __forceinline__ void team_bar(uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
 template <bool PAGED>
-__global__ void __launch_bounds__(kThinTeamsMax * 128)
+__global__ void __launch_bounds__(kThinTeams * 128, 2)
 k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
           uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
-  __shared__ uint32_t s_nesc[kThinTeamsMax];
+  __shared__ uint32_t s_nesc[kThinTeams];
   uint16_t *cdfr = reinterpret_cast<uint16_t *>(smb + kThinCdf);
   const int nteams = int(blockDim.x >> 7);
 
@@ -1029,7 +1031,7 @@ k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restri
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
 
-  if (threadIdx.x < kThinTeamsMax) s_nesc[threadIdx.x] = 0;
+  if (threadIdx.x < kThinTeams) s_nesc[threadIdx.x] = 0;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
@@ -1156,7 +1158,7 @@ k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restri
       // ---- symbol: the pair of the lane's bucket (fine at the tails)
       const uint32_t slot = x & 0xFFFFu;
       const uint32_t sm8 = smb[mcol + ((x >> 1) & 0x7F80u)];  // row slot >> 8
-      const uint32_t sf8 = smb[fcol + ((x << 2) & 0x3F80u)];  // row (slot >> 5) & 127: both tails
+      const uint32_t sf8 = smb[fcol + ((x << 2) & 0x1F80u)];  // row (slot >> 5) & 63: both tails
       const uint32_t sa = ((slot + kThinTail) & 0xFFFFu) < 2 * kThinTail ? sf8 : sm8;
       const uint32_t cb = ccol + sa * 256;
       const uint32_t c0 = lds16(smb, cb), c1 = lds16(smb, cb + 256), c2 = lds16(smb, cb + 512);
@@ -1273,30 +1275,27 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
   return cudaGetLastError();
 }
 
-// Thin ranges: a CTA per (level, head, `teams` of the level's chunks); CTAs
-// past the level's chunk count return at once.  Two teams: two CTAs share
-// an SM; eight: one CTA holds eight streams of a level on the SM's one table.
+// Thin ranges: a CTA per (level, head, four of the level's chunks), two
+// CTAs per SM; CTAs past the level's chunk count return at once.
 template <bool PAGED>
 cudaError_t launch_decode_thin(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
-                               uint8_t *ws, int chunks, int teams, cudaStream_t st, const PagedOut &po, int l0,
-                               int l1) {
-  const int smem = int(thin_smem(teams));
-  cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(thin_smem(kThinTeamsMax)));
+                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+  const int smem = int(thin_smem(kThinTeams));
+  cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
     e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              int(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + teams - 1) / teams);
-  k_thin128<PAGED><<<grid, teams * 128, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kThinTeams - 1) / kThinTeams);
+  k_thin128<PAGED><<<grid, kThinTeams * 128, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
+                                                          l1 * 2 * lo.H);
   return cudaGetLastError();
 }
 
-// chunks: the chunks in the range.  d = 128: when the levels share the
-// range thinly (a mean of at most two chunks per level), the thin-range
-// kernel with two teams per CTA, two CTAs per SM; with at most eight per
-// level in a range of at most 16 chunks, the thin-range kernel with eight
-// teams per CTA; otherwise k_dec128, a warp per chunk.  Other d: k_decode,
+// chunks: the chunks in the range.  d = 128: when the range holds a mean
+// of at most kThinPerLevel chunks per level, the thin-range kernel;
+// otherwise k_dec128, a warp per chunk (which wins once a level's chunks
+// need several four-team CTAs, each building the tables).  Other d: k_decode,
 // a team per chunk of the CTA's level, and at least 512 threads so that the
 // table build is spread wide (teams without a chunk only build).
 template <int T, bool PAGED>
@@ -1305,10 +1304,7 @@ cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint
                              int l0, int l1) {
   if constexpr (T == 32) {
     const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
-    if (per_level <= 2)
-      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, 2, st, po, l0, l1);
-    if (per_level <= 8 && chunks <= 16)
-      return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, 8, st, po, l0, l1);
+    if (per_level <= kThinPerLevel) return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
     return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
   } else {
     constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
