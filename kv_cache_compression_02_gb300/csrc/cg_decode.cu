@@ -20,7 +20,9 @@
 //                   fma(q, step, a_hat) is clamped, converted to fp16 and
 //                   stored 8 bytes per thread (a team writes one token row).
 //   k_dec128        (d = 128) the same with a warp per chunk stream and
-//                   tables laid out for a short token loop.
+//                   tables laid out for a short token loop; for ranges with
+//                   a few chunks per level (MID) with u8 pair tables, so
+//                   that two CTAs share an SM.
 //   k_thin128       (d = 128, chunk ranges that give each (level, head) only
 //                   a few chunks) four warps per stream, one lane per
 //                   thread, for a short dependency chain per token.
@@ -591,6 +593,18 @@ constexpr uint32_t kRingOff = kCdfOff + kCdfRows * 256; // rings [teams][kRing +
 constexpr uint32_t kRingStride = kRing + kMirror;       // words per warp ring
 constexpr uint32_t kTail = 2048;                        // slots covered by the fine table at each end
 constexpr int kTeams128Max = 24;
+// MID (ranges with a few chunks per level): u8 pair tables as k_thin128's,
+// in this kernel's column order (lane 4 i + j at byte 4 i + j, bank i), so
+// that two CTAs of eight teams share an SM.
+constexpr uint32_t kMidFine = 0;                       // fine [64][128] u8: 32-slot buckets, 1024-slot tails
+constexpr uint32_t kMidMain = kMidFine + 64 * 128;     // main [248][128] u8: 256-slot buckets of [1024, 64512)
+constexpr uint32_t kMidCdf = kMidMain + 248 * 128;     // cdfc [258][128] u16
+constexpr uint32_t kMidRing = kMidCdf + kCdfRows * 256;
+constexpr int kMidTeams = 8;
+template <bool MID>
+__host__ __device__ constexpr uint32_t cdf_off() { return MID ? kMidCdf : kCdfOff; }
+template <bool MID>
+__host__ __device__ constexpr uint32_t ring_off() { return MID ? kMidRing : kRingOff; }
 
 // byte offset of lane j of thread 0 in a table row (thread i adds 4 i)
 template <int J>
@@ -672,7 +686,7 @@ __device__ __forceinline__ void build_pairs(uint16_t *lut, const uint16_t *cdfc,
 // escape symbol, whose frequency reads as 0): a binary search of the lane's
 // cdf column.  Replaces the lane's frequency, offset in range and symbol
 // row (symbol << 8); marks an escape in escm.
-template <int J>
+template <int J, uint32_t CDF>
 __device__ __forceinline__ void slow128(const uint8_t *sm, uint32_t i4, uint32_t x, uint32_t &ff, uint32_t &rr,
                                         uint32_t &ro, uint32_t &escm) {
   const uint32_t col = i4 + colb<J>();
@@ -680,28 +694,29 @@ __device__ __forceinline__ void slow128(const uint8_t *sm, uint32_t i4, uint32_t
   uint32_t s = 0;  // largest s with cdf_s <= slot (cdf_0 = 0)
 #pragma unroll
   for (uint32_t stp = 128; stp; stp >>= 1)
-    if (lds16(sm, kCdfOff + ((s + stp) << 8) + col) <= slot) s += stp;
-  const uint32_t c0 = lds16(sm, kCdfOff + (s << 8) + col);
-  const uint32_t c1 = s < 255 ? lds16(sm, kCdfOff + ((s + 1) << 8) + col) : kM;
+    if (lds16(sm, CDF + ((s + stp) << 8) + col) <= slot) s += stp;
+  const uint32_t c0 = lds16(sm, CDF + (s << 8) + col);
+  const uint32_t c1 = s < 255 ? lds16(sm, CDF + ((s + 1) << 8) + col) : kM;
   ff = c1 - c0;
   rr = slot - c0;
   ro = s << 8;
   if (s == uint32_t(kEsc)) escm |= 1u << J;
 }
 
-template <bool PAGED>
-__global__ void __launch_bounds__(kTeams128Max * 32, 1)
+template <bool PAGED, bool MID>
+__global__ void __launch_bounds__(MID ? kMidTeams * 32 : kTeams128Max * 32, MID ? 2 : 1)
 k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
   constexpr int T = 32;
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
-  uint16_t *cdfc = reinterpret_cast<uint16_t *>(smb + kCdfOff);
+  uint16_t *cdfc = reinterpret_cast<uint16_t *>(smb + cdf_off<MID>());
 
   const int lv = blockIdx.x, si = blockIdx.y;
   if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
-  if (cnt == 0) return;
+  const int nteams = blockDim.x >> 5, first = int(blockIdx.z) * nteams;  // this CTA's entries of the list
+  if (first >= cnt) return;
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
@@ -712,24 +727,36 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
                         tab_index(lo, lv, l, kvi, h * lo.d) * 256;
   build_cdf_columns<T>(cdf, cdfc, &s_bad);
   __syncthreads();
-  // main entries of the tail buckets (the first and last 8) point to the fine table
-  build_pairs(reinterpret_cast<uint16_t *>(smb + kMainOff), cdfc, 256, 256, 0, kTail / 256, 256 - kTail / 256);
-  build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff), cdfc, 128, 16, 0, 0, 128);
-  build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff) + 128 * 128, cdfc, 128, 16, kM - kTail, 0, 128);
+  if constexpr (MID) {
+    // the lane at cdf position p owns byte chan_of(p) of a u8 row
+    const auto sa8 = [&](uint8_t *lut) {
+      return [lut](uint32_t b, uint32_t p, uint32_t sa, uint32_t, uint32_t) {
+        lut[b * 128 + chan_of<T>(int(p))] = uint8_t(min(sa, 254u));
+      };
+    };
+    build_buckets(cdfc, 248, 256, 1024, sa8(smb + kMidMain));
+    build_buckets(cdfc, 32, 32, 0, sa8(smb + kMidFine));
+    build_buckets(cdfc, 32, 32, kM - 1024, sa8(smb + kMidFine + 32 * 128));
+  } else {
+    // main entries of the tail buckets (the first and last 8) point to the fine table
+    build_pairs(reinterpret_cast<uint16_t *>(smb + kMainOff), cdfc, 256, 256, 0, kTail / 256, 256 - kTail / 256);
+    build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff), cdfc, 128, 16, 0, 0, 128);
+    build_pairs(reinterpret_cast<uint16_t *>(smb + kFineOff) + 128 * 128, cdfc, 128, 16, kM - kTail, 0, 128);
+  }
   __syncthreads();
   if (s_bad) {
     if (threadIdx.x == 0) atomicOr(status, kStCorrupt);
     return;
   }
 
-  const int team = threadIdx.x >> 5, nteams = blockDim.x >> 5;
+  const int team = threadIdx.x >> 5;
   const uint32_t i = threadIdx.x & 31, i4 = 4 * i;
   const float4 st4 = *reinterpret_cast<const float4 *>(
       reinterpret_cast<const float *>(tables + lo.tb_step) + tab_index(lo, lv, l, kvi, h * lo.d + i4));
   const float step[4] = {st4.x, st4.y, st4.z, st4.w};
-  uint16_t *ring = reinterpret_cast<uint16_t *>(smb + kRingOff) + team * kRingStride;
+  uint16_t *ring = reinterpret_cast<uint16_t *>(smb + ring_off<MID>()) + team * kRingStride;
 
-  for (int idx = team; idx < cnt; idx += nteams) {
+  for (int idx = first + team; idx < cnt; idx += nteams * int(gridDim.z)) {
     const int k = list[idx];
     const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k), nd = chunk_nd(lo, k);
     const uint64_t base = ld_u64(buf + 64 + 8 * uint64_t(k));
@@ -849,18 +876,48 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
     ro[J] = t & 0xFF00u;                                                      \
     sl[J] = rr[J] >= ff[J];                                                   \
   }
-        CG_LOOKUP(0)
-        CG_LOOKUP(1)
-        CG_LOOKUP(2)
-        CG_LOOKUP(3)
+// MID: the pair's first symbol sa from the u8 tables (the fine one at the
+// 1024-slot tails; the main row of a tail slot falls on the fine table or
+// the cdf rows, in bounds, and is not used), then cdf_sa, cdf_sa+1 and
+// cdf_sa+2 pick sa or sa + 1.
+#define CG_LOOKUP_MID(J)                                                               \
+  {                                                                                    \
+    const uint32_t xx = x[J];                                                          \
+    const uint32_t slot = xx & 0xFFFFu;                                                \
+    const uint32_t sm8 = smb[kMidMain - 4 * 128 + i4 + J + ((xx >> 1) & 0x7F80u)];     \
+    const uint32_t sf8 = smb[kMidFine + i4 + J + ((xx << 2) & 0x1F80u)];               \
+    const uint32_t sa = ((slot + 1024u) & 0xFFFFu) < 2048u ? sf8 : sm8;                \
+    const uint32_t r = (sa << 8) | i4;                                                 \
+    const uint32_t c0 = lds16(smb, kMidCdf + colb<J>() + r);                           \
+    const uint32_t c1 = lds16(smb, kMidCdf + 256 + colb<J>() + r);                     \
+    const uint32_t c2 = lds16(smb, kMidCdf + 512 + colb<J>() + r);                     \
+    const bool up = slot >= c1;                                                        \
+    const uint32_t clo = up ? c1 : c0;                                                 \
+    ff[J] = (up ? c2 : c1) - clo;                                                      \
+    rr[J] = slot - clo;                                                                \
+    ro[J] = (sa + (up ? 1u : 0u)) << 8;                                                \
+    sl[J] = rr[J] >= ff[J];                                                            \
+  }
+        if constexpr (MID) {
+          CG_LOOKUP_MID(0)
+          CG_LOOKUP_MID(1)
+          CG_LOOKUP_MID(2)
+          CG_LOOKUP_MID(3)
+        } else {
+          CG_LOOKUP(0)
+          CG_LOOKUP(1)
+          CG_LOOKUP(2)
+          CG_LOOKUP(3)
+        }
 #undef CG_LOOKUP
+#undef CG_LOOKUP_MID
         uint32_t escm = 0, cntw = 0;
         bool esc_warp = false;
         if (__any_sync(0xffffffffu, sl[0] | sl[1] | sl[2] | sl[3])) {
-          if (sl[0]) slow128<0>(smb, i4, x[0], ff[0], rr[0], ro[0], escm);
-          if (sl[1]) slow128<1>(smb, i4, x[1], ff[1], rr[1], ro[1], escm);
-          if (sl[2]) slow128<2>(smb, i4, x[2], ff[2], rr[2], ro[2], escm);
-          if (sl[3]) slow128<3>(smb, i4, x[3], ff[3], rr[3], ro[3], escm);
+          if (sl[0]) slow128<0, cdf_off<MID>()>(smb, i4, x[0], ff[0], rr[0], ro[0], escm);
+          if (sl[1]) slow128<1, cdf_off<MID>()>(smb, i4, x[1], ff[1], rr[1], ro[1], escm);
+          if (sl[2]) slow128<2, cdf_off<MID>()>(smb, i4, x[2], ff[2], rr[2], ro[2], escm);
+          if (sl[3]) slow128<3, cdf_off<MID>()>(smb, i4, x[3], ff[3], rr[3], ro[3], escm);
           cntw = 2 * __popc(escm);  // an escape's raw value takes two words
           esc_warp = __any_sync(0xffffffffu, escm != 0);
         }
@@ -984,7 +1041,8 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 // halves that the team's first warp refills; a token whose words reach past
 // those known to have landed waits for them, behind one more barrier.
 constexpr int kThinTeams = 4;                                   // teams (streams) per CTA, 128 threads each
-constexpr int kThinPerLevel = 6;                                // thin launches: mean chunks per level at most this
+constexpr int kThinPerLevel = 4;                                // thin launches: mean chunks per level at most this
+constexpr int kMidPerLevel = 8;                                 // MID launches (k_dec128 with u8 tables): at most this
 constexpr uint32_t kThinTail = 1024;                            // slots with fine buckets, at each end
 constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 248
 constexpr uint32_t kThinFineRows = 2 * kThinTail / 32;          // 64
@@ -994,6 +1052,7 @@ constexpr uint32_t kThinCdf = kThinMain + kThinMainRows * 128;
 constexpr uint32_t kThinRing = kThinCdf + kCdfRows * 256;  // rings [teams][kRing] u16, then word counts [teams][2][4] u32
 __host__ __device__ constexpr uint32_t thin_smem(int teams) { return kThinRing + uint32_t(teams) * (kRing * 2 + 32); }
 static_assert(thin_smem(kThinTeams) + 64 + 1024 <= 233472 / 2, "two thin CTAs must share an SM");
+static_assert(kMidRing + kMidTeams * kRingStride * 2 + 64 + 1024 <= 233472 / 2, "two MID CTAs must share an SM");
 
 // The thin tables' column of lane 32 w + t: u16 position p = 2 t + 64 (w >> 1)
 // + (w & 1) of a cdf row, and the lane and u8 byte of position p.
@@ -1268,10 +1327,28 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
   const int teams = chunks > kTeams128Max ? kTeams128Max : (chunks < 16 ? 16 : chunks);
   const size_t smem = kRingOff + size_t(teams) * kRingStride * 2;
-  cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
-  k_dec128<PAGED><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  k_dec128<PAGED, false><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  return cudaGetLastError();
+}
+
+// d = 128, ranges with a few chunks per level: k_dec128 with the u8 pair
+// tables, a CTA per (level, head, eight of the level's chunks), two CTAs per
+// SM; CTAs past the level's chunk count return at once.
+template <bool PAGED>
+cudaError_t launch_decode_mid(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
+                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+  const size_t smem = kMidRing + size_t(kMidTeams) * kRingStride * 2;
+  cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
+    e = cudaFuncSetAttribute(k_dec128<PAGED, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kMidTeams - 1) / kMidTeams);
+  k_dec128<PAGED, true><<<grid, kMidTeams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
+                                                             l1 * 2 * lo.H);
   return cudaGetLastError();
 }
 
@@ -1292,10 +1369,12 @@ cudaError_t launch_decode_thin(const Layout &lo, const uint8_t *tables, const ui
   return cudaGetLastError();
 }
 
-// chunks: the chunks in the range.  d = 128: when the range holds a mean
-// of at most kThinPerLevel chunks per level, the thin-range kernel;
-// otherwise k_dec128, a warp per chunk (which wins once a level's chunks
-// need several four-team CTAs, each building the tables).  Other d: k_decode,
+// chunks: the chunks in the range.  d = 128, by the mean chunks per level
+// (crossovers measured on the 70B and 128K workloads): at most four, the
+// thin-range kernel (four warps per stream, a short token); at most eight,
+// k_dec128 with the u8 pair tables and eight warps per CTA, two CTAs per SM;
+// otherwise k_dec128 with its full tables and a warp per chunk of the level.
+// Other d: k_decode,
 // a team per chunk of the CTA's level, and at least 512 threads so that the
 // table build is spread wide (teams without a chunk only build).
 template <int T, bool PAGED>
@@ -1305,6 +1384,7 @@ cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint
   if constexpr (T == 32) {
     const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
     if (per_level <= kThinPerLevel) return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
+    if (per_level <= kMidPerLevel) return launch_decode_mid<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
     return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
   } else {
     constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;

@@ -3,9 +3,9 @@ output KV in pinned host memory mapped into the device address space, so
 the decoder reads the words and writes the tokens across the host link
 (the receiver decodes a streamed context as it arrives: Guide to CacheGen,
 pillar 4).  Every result must equal the oracle's decode, bit for bit, with
-each d = 128 decoder (a warp per stream for 15 chunks; the thin-range
-kernel for a 3-chunk range with eight teams per CTA and for a 2-chunk range
-with two)."""
+each d = 128 decoder (a warp per stream with the full tables for 15
+chunks and with the u8 tables for 6; the thin-range kernel for a 3-chunk and
+a 2-chunk range)."""
 import numpy as np
 import pytest
 
@@ -66,7 +66,7 @@ def test_full_decode_host_to_host(orc, case):
     assert np.array_equal(_run(case, 0, -1), want)
 
 
-@pytest.mark.parametrize("k0,k1", [(4, 7), (13, 15)])
+@pytest.mark.parametrize("k0,k1", [(4, 7), (13, 15), (2, 8)])
 def test_chunk_range_host_to_host_writes_only_its_tokens(orc, case, k0, k1):
     spec, cfg, tb, cont = case
     rc, ref = orc.decode(tb, cont, k0, k1)

@@ -25,6 +25,10 @@ CASES = {
                                            n_outliers=1), 64, 10, (0.05, 0.4), [1, 0, 1, 1, 0], 1, 0, (0, -1)),
     "d64_one_block_longer_than_S": (synth.GenSpec(L=1, H=2, d=64, S=250, seed=44), 100, 10, (0.1,), None, 512, 2,
                                     (0, -1)),
+    # d = 128, six chunks of one level: a warp per stream with the u8 tables
+    "d128_bt16_mid_range": (synth.GenSpec(L=2, H=2, d=128, S=1500, seed=46, innov="t3", rho=(0.85, 0.99),
+                                          n_outliers=1, outlier_scale=20.0), 256, 10, (0.1,), None, 16, 4,
+                            (0, -1)),
     # d = 128, four chunks of two levels: the thin-range decoder
     "d128_bt16_thin_range": (synth.GenSpec(L=2, H=2, d=128, S=1500, seed=45, innov="t3", rho=(0.85, 0.99),
                                            n_outliers=1, outlier_scale=20.0), 256, 10, (0.1, 0.3),

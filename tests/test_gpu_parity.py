@@ -57,6 +57,10 @@ CASES = {
     # so tokens whose words outrun the staging ring come up too
     "d128_thin_escapes_R3": (synth.GenSpec(L=1, H=2, d=128, S=200, seed=33, innov="t3", rho=(0.85, 0.9)),
                              100, 10, 3, (0.05,), None, None),
+    # d = 128, six chunks of one level: k_dec128 with the u8 pair tables,
+    # eight warps per CTA (MID); the last chunk is ragged
+    "d128_mid_six_chunks": (synth.GenSpec(L=2, H=2, d=128, S=5 * 128 + 77, seed=35, innov="t3", rho=(0.85, 0.99),
+                                          n_outliers=2, outlier_scale=20.0), 128, 10, 127, (0.05,), None, None),
     # eight chunks over four levels, two each; the last chunk is ragged
     "d128_thin_mixed_ragged": (synth.GenSpec(L=2, H=2, d=128, S=1000, seed=34, innov="t3", rho=(0.85, 0.99),
                                              n_outliers=2, outlier_scale=20.0), 128, 10, 127,
@@ -113,9 +117,8 @@ def test_chunk_range_decode(orc):
 
 
 def test_chunk_range_decode_d128(orc):
-    """Small chunk ranges at d = 128 (the thin-range decoder, with two and
-    with eight teams per CTA): each equals the oracle's decode of that range,
-    and no other token is written."""
+    """Small chunk ranges at d = 128 (the thin-range decoder): each equals the
+    oracle's decode of that range, and no other token is written."""
     x, cd, cfg, levels, lb, lm = _setup(orc, "d128_thin_mixed_ragged")
     rc, tb = orc.fit_tables(cd, list(lb), lm, x)
     rc, cont, _ = orc.encode(cd, len(lb), tb, x, levels)
@@ -155,10 +158,11 @@ def _small(orc, name="d8_group7"):
     return x, cd, cfg, levels, tb, cont
 
 
-# d = 8; d = 128 with 3 chunks (thin-range decoder, eight teams); d = 128 with
-# 42 chunks (a warp per stream); d = 128 with two chunks per level (thin-range
-# decoder, two teams)
-@pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams", "d128_thin_mixed_ragged"])
+# d = 8; d = 128 with 3 chunks (thin-range decoder); d = 128 with 42 chunks
+# (a warp per stream, full tables); d = 128 with two chunks per level
+# (thin-range decoder); d = 128 with six chunks (a warp per stream, u8 tables)
+@pytest.mark.parametrize("name", ["d8_group7", "d128_ragged_chunks", "many_chunks_teams", "d128_thin_mixed_ragged",
+                                  "d128_mid_six_chunks"])
 def test_corrupt_containers_flagged(orc, name):
     x, cd, cfg, levels, tb, cont = _small(orc, name)
     assert gu.decode(cfg, tb, cont)[0] == cg.CG_OK
