@@ -353,10 +353,15 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
     const int64_t ta = t0 + int64_t(g) * lo.G;
     const int te = int(min(ta + lo.G, t0 + chunk_ntok(lo, k)) - ta);  // rows of the group
     const float4 *sp = reinterpret_cast<const float4 *>(scale + (uint64_t(k) * lo.nstr + si) * lo.d + c0);
-    const float4 s01 = sp[0], s23 = sp[1];  // (s, 127/absmax) of the four channels
-    const float sc[4] = {s01.x, s01.z, s23.x, s23.z}, inv[4] = {s01.y, s01.w, s23.y, s23.w};
     const uint2 *grow = head + ta * tpr;
+    // the scales, the anchor row and the first nine delta rows are loaded
+    // together: one memory round trip for a group of up to ten tokens
+    const float4 s01 = sp[0], s23 = sp[1];  // (s, 127/absmax) of the four channels
     const uint2 wa = __ldg(grow);
+    uint2 w9[9];
+#pragma unroll
+    for (int u = 0; u < 9; u++) w9[u] = 1 + u < te ? __ldg(grow + (1 + u) * tpr) : make_uint2(0, 0);
+    const float sc[4] = {s01.x, s01.z, s23.x, s23.z}, inv[4] = {s01.y, s01.w, s23.y, s23.w};
     const uint32_t ha[4] = {wa.x & 0xFFFFu, wa.x >> 16, wa.y & 0xFFFFu, wa.y >> 16};
     float ah[4];
 #pragma unroll
@@ -364,22 +369,28 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
       const int a = max(-127, min(127, __float2int_rn(__fmul_rn(__half2float(__ushort_as_half(uint16_t(ha[i]))), inv[i]))));
       ah[i] = __fmul_rn(float(a), sc[i]);
     }
-    for (int tb = 1; tb < te; tb += 8) {  // 8 rows in flight
+#define CG_COUNT_ROW(W)                                                                                   \
+  {                                                                                                       \
+    const uint32_t hw[4] = {(W).x & 0xFFFFu, (W).x >> 16, (W).y & 0xFFFFu, (W).y >> 16};                 \
+    _Pragma("unroll") for (int i = 0; i < 4; i++) {                                                       \
+      const int q =                                                                                       \
+          __float2int_rn(__fmul_rn(__fsub_rn(__half2float(__ushort_as_half(uint16_t(hw[i]))), ah[i]), rc[i])); \
+      const int sym = uint32_t(q) + R <= 2 * R ? q + 127 : kEsc; /* |q| <= R as one unsigned compare */  \
+      atomicAdd(&hrow[i][sym], 1u);                                                                       \
+    }                                                                                                     \
+  }
+#pragma unroll
+    for (int u = 0; u < 9; u++)
+      if (1 + u < te) CG_COUNT_ROW(w9[u])
+    for (int tb = 10; tb < te; tb += 8) {  // groups of more than ten tokens: 8 more rows in flight at a time
       uint2 w8[8];
 #pragma unroll
       for (int u = 0; u < 8; u++) w8[u] = tb + u < te ? __ldg(grow + (tb + u) * tpr) : make_uint2(0, 0);
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
-        if (tb + u >= te) break;
-        const uint32_t hw[4] = {w8[u].x & 0xFFFFu, w8[u].x >> 16, w8[u].y & 0xFFFFu, w8[u].y >> 16};
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const int q = __float2int_rn(__fmul_rn(__fsub_rn(__half2float(__ushort_as_half(uint16_t(hw[i]))), ah[i]), rc[i]));
-          const int sym = uint32_t(q) + R <= 2 * R ? q + 127 : kEsc;  // |q| <= R as one unsigned compare
-          atomicAdd(&hrow[i][sym], 1u);
-        }
-      }
+      for (int u = 0; u < 8; u++)
+        if (tb + u < te) CG_COUNT_ROW(w8[u])
     }
+#undef CG_COUNT_ROW
   }
   __syncthreads();
 
