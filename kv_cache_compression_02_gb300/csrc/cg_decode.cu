@@ -703,10 +703,12 @@ __device__ __forceinline__ void slow128(const uint8_t *sm, uint32_t i4, uint32_t
   if (s == uint32_t(kEsc)) escm |= 1u << J;
 }
 
+// cmin, cmax: the CTA decodes its level only if the level holds that many
+// chunks in the range (the launches for the other counts take the rest).
 template <bool PAGED, bool MID>
 __global__ void __launch_bounds__(MID ? kMidTeams * 32 : kTeams128Max * 32, MID ? 2 : 1)
 k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
-         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
+         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi, int cmin, int cmax) {
   constexpr int T = 32;
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
@@ -716,7 +718,7 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
   const int nteams = blockDim.x >> 5, first = int(blockIdx.z) * nteams;  // this CTA's entries of the list
-  if (first >= cnt) return;
+  if (cnt < cmin || cnt > cmax || first >= cnt) return;
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
@@ -1041,7 +1043,7 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
 // halves that the team's first warp refills; a token whose words reach past
 // those known to have landed waits for them, behind one more barrier.
 constexpr int kThinTeams = 4;                                   // teams (streams) per CTA, 128 threads each
-constexpr int kThinPerLevel = 4;                                // thin launches: mean chunks per level at most this
+constexpr int kThinPerLevel = 4;                                // thin launches: levels of at most this many chunks
 constexpr int kMidPerLevel = 8;                                 // MID launches (k_dec128 with u8 tables): at most this
 constexpr uint32_t kThinTail = 1024;                            // slots with fine buckets, at each end
 constexpr uint32_t kThinMainRows = (kM - 2 * kThinTail) / 256;  // 248
@@ -1074,7 +1076,7 @@ __device__ __forceinline__ void team_bar(uint32_t id) { asm volatile("bar.sync %
 template <bool PAGED>
 __global__ void __launch_bounds__(kThinTeams * 128, 2)
 k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
-          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi) {
+          uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi, int cmin, int cmax) {
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
   __shared__ uint32_t s_nesc[kThinTeams];
@@ -1085,7 +1087,7 @@ k_thin128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restri
   if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
   const int first = int(blockIdx.z) * nteams;  // this CTA's entries of the level's chunk list
-  if (first >= cnt) return;
+  if (cnt < cmin || cnt > cmax || first >= cnt) return;  // (cmin, cmax: as for k_dec128)
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
@@ -1324,13 +1326,15 @@ cudaError_t launch_decode_tpb(const Layout &lo, const uint8_t *tables, const uin
 // a chunk only build).
 template <bool PAGED>
 cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
-                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1,
+                              int cmin, int cmax) {
   const int teams = chunks > kTeams128Max ? kTeams128Max : (chunks < 16 ? 16 : chunks);
   const size_t smem = kRingOff + size_t(teams) * kRingStride * 2;
   cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
-  k_dec128<PAGED, false><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H);
+  k_dec128<PAGED, false><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H,
+                                                         cmin, cmax);
   return cudaGetLastError();
 }
 
@@ -1339,16 +1343,17 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
 // SM; CTAs past the level's chunk count return at once.
 template <bool PAGED>
 cudaError_t launch_decode_mid(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
-                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+                              uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1,
+                              int cmin, int cmax) {
   const size_t smem = kMidRing + size_t(kMidTeams) * kRingStride * 2;
   cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
     e = cudaFuncSetAttribute(k_dec128<PAGED, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              int(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kMidTeams - 1) / kMidTeams);
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (min(chunks, cmax) + kMidTeams - 1) / kMidTeams);
   k_dec128<PAGED, true><<<grid, kMidTeams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
-                                                             l1 * 2 * lo.H);
+                                                             l1 * 2 * lo.H, cmin, cmax);
   return cudaGetLastError();
 }
 
@@ -1356,25 +1361,28 @@ cudaError_t launch_decode_mid(const Layout &lo, const uint8_t *tables, const uin
 // CTAs per SM; CTAs past the level's chunk count return at once.
 template <bool PAGED>
 cudaError_t launch_decode_thin(const Layout &lo, const uint8_t *tables, const uint8_t *buf, uint16_t *kv,
-                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1) {
+                               uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po, int l0, int l1,
+                               int cmin, int cmax) {
   const int smem = int(thin_smem(kThinTeams));
   cudaError_t e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
     e = cudaFuncSetAttribute(k_thin128<PAGED>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              int(cudaSharedmemCarveoutMaxShared));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (chunks + kThinTeams - 1) / kThinTeams);
+  dim3 grid(lo.n_levels, l1 * 2 * lo.H, (min(chunks, cmax) + kThinTeams - 1) / kThinTeams);
   k_thin128<PAGED><<<grid, kThinTeams * 128, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
-                                                          l1 * 2 * lo.H);
+                                                          l1 * 2 * lo.H, cmin, cmax);
   return cudaGetLastError();
 }
 
-// chunks: the chunks in the range.  d = 128, by the mean chunks per level
-// (crossovers measured on the 70B and 128K workloads): at most four, the
-// thin-range kernel (four warps per stream, a short token); at most eight,
-// k_dec128 with the u8 pair tables and eight warps per CTA, two CTAs per SM;
-// otherwise k_dec128 with its full tables and a warp per chunk of the level.
-// Other d: k_decode,
+// chunks: the chunks in the range.  d = 128: each level goes to the kernel
+// measured best for the chunks it holds in the range (crossovers on the 70B
+// and 128K workloads), which only the device knows (k_decode_index counts
+// them): at most four, the thin-range kernel (four warps per stream, a short
+// token); five to eight, k_dec128 with the u8 pair tables and eight warps
+// per CTA, two CTAs per SM; more, k_dec128 with its full tables and a warp
+// per chunk of the level.  One launch per band that the range can reach;
+// a CTA whose level is in another band returns at once.  Other d: k_decode,
 // a team per chunk of the CTA's level, and at least 512 threads so that the
 // table build is spread wide (teams without a chunk only build).
 template <int T, bool PAGED>
@@ -1382,10 +1390,14 @@ cudaError_t launch_decode_tp(const Layout &lo, const uint8_t *tables, const uint
                              uint16_t *kv, uint8_t *ws, int chunks, cudaStream_t st, const PagedOut &po,
                              int l0, int l1) {
   if constexpr (T == 32) {
-    const int per_level = (chunks + lo.n_levels - 1) / lo.n_levels;
-    if (per_level <= kThinPerLevel) return launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
-    if (per_level <= kMidPerLevel) return launch_decode_mid<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
-    return launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1);
+    cudaError_t e = cudaSuccess;
+    if (chunks > kMidPerLevel)
+      e = launch_decode_128<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1, kMidPerLevel + 1, chunks);
+    if (e == cudaSuccess && chunks > kThinPerLevel)
+      e = launch_decode_mid<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1, kThinPerLevel + 1, kMidPerLevel);
+    if (e == cudaSuccess)
+      e = launch_decode_thin<PAGED>(lo, tables, buf, kv, ws, chunks, st, po, l0, l1, 1, kThinPerLevel);
+    return e;
   } else {
     constexpr int kTeamsMax = max_threads<T>() / T, kTeamsMin = (512 / T < kTeamsMax) ? 512 / T : kTeamsMax;
     const int teams = chunks > kTeamsMax ? kTeamsMax : (chunks < kTeamsMin ? kTeamsMin : chunks);
