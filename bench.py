@@ -700,6 +700,9 @@ def main():
     dec_alg = sum(nbytes_list) + nsets * fp16
     enc_alg = nsets * fp16 + sum(nbytes_list)
     dec_ach = dec_alg / (ms["dec"] * 1e-3) / 1e9
+    # per step: fit 3 launches, encode 6 per container, decode the index and,
+    # at d = 128, one launch per band of chunks per level the range can reach
+    dec_launches = 1 + ((1 + (w.n_chunks > 4) + (w.n_chunks > 8)) if w.d == 128 else 1)
     enc_ach = enc_alg / (ms["enc"] * 1e-3) / 1e9
     tb_bytes = tables.numel()
 
@@ -760,7 +763,7 @@ def main():
         "decode_layer_groups": lgroups,
         "decode_streamed": streamed,
         "adaptive_streaming": adaptive,
-        "gpu_launches": args.steps * (3 + nsets * (6 + 2)),
+        "gpu_launches": args.steps * (3 + nsets * (6 + dec_launches)),
         "clocks": clk,
         "cpu_baseline": cpu,
         "setup": {"generate_s": gen_s},
