@@ -624,41 +624,54 @@ __device__ __forceinline__ uint32_t scan_step(uint32_t v) {
   return v;
 }
 
-// Bucket entries for the d = 128 tables (cdf rows of 128 u16 positions), one
-// thread per (bucket, position) with the position fastest, so that a warp's
-// threads read different banks, and four entries in flight per thread: the
-// symbol at the bucket's first slot by a binary search of the position's cdf
-// column, then the first symbol sa of the neighbouring pair holding most of
-// the bucket's `width` slots.  emit(b, p, sa, nxt, slot0) writes the entry
-// of bucket b (first slot slot0) at position p; nxt = cdf_(sa+1) (M for
+// Bucket entries for the d = 128 tables (cdf rows of 128 u16 positions).  A
+// thread takes kG consecutive buckets of one position, positions fastest so
+// that a warp's threads read different banks: a binary search of the
+// position's cdf column for the symbol at the first bucket's first slot, then
+// per bucket a walk over the symbols it holds for the first symbol sa of the
+// neighbouring pair holding most of its `width` slots, carrying the symbol at
+// the bucket's end to the next bucket.  emit(b, p, sa, nxt, slot0) writes the
+// entry of bucket b (first slot slot0) at position p; nxt = cdf_(sa+1) (M for
 // sa = 255).
 template <typename Emit>
 __device__ __forceinline__ void build_buckets(const uint16_t *cdfc, int nb, uint32_t width, uint32_t base,
                                               Emit emit) {
-  constexpr int kRowU = 128, kU = 4;
-  const int n = nb * kRowU;
-  for (int e0 = threadIdx.x; e0 < n; e0 += kU * int(blockDim.x)) {
-    uint32_t s[kU];  // largest s with cdf_s <= the bucket's first slot (cdf_0 = 0)
+  constexpr int kRowU = 128, kG = 8;
+  const int n = (nb + kG - 1) / kG * kRowU;
+  for (int e = threadIdx.x; e < n; e += int(blockDim.x)) {
+    const uint32_t p = e % kRowU, b0 = e / kRowU * kG;
+    const uint16_t *colp = cdfc + p;
+    uint32_t slot0 = base + width * b0;
+    uint32_t s = 0;  // largest s with cdf_s <= slot0 (cdf_0 = 0)
 #pragma unroll
-    for (int u = 0; u < kU; u++) s[u] = 0;
-#pragma unroll
-    for (uint32_t stp = 128; stp; stp >>= 1) {
-#pragma unroll
-      for (int u = 0; u < kU; u++) {
-        const int e = min(e0 + u * int(blockDim.x), n - 1);  // (past the end: a repeat, never emitted)
-        const uint32_t slot0 = base + width * uint32_t(e / kRowU);
-        if (s[u] + stp <= 255 && cdfc[(s[u] + stp) * kRowU + e % kRowU] <= slot0) s[u] += stp;
+    for (uint32_t stp = 128; stp; stp >>= 1)
+      if (s + stp <= 255 && colp[(s + stp) * kRowU] <= slot0) s += stp;
+    uint32_t cs1 = s < 255 ? uint32_t(colp[(s + 1) * kRowU]) : kM;  // cdf_(s+1)
+    for (uint32_t b = b0; b < b0 + kG && int(b) < nb; b++) {
+      const uint32_t end = slot0 + width;
+      uint32_t t = s, nt = cs1, beg = slot0, prev = 0, best = 0, sa = s, nxt = cs1;
+      for (;;) {
+        const uint32_t cnt = min(nt, end) - beg;  // in-bucket slots of t
+        if (t > s && prev + cnt > best) {
+          best = prev + cnt;
+          sa = t - 1;
+          nxt = beg;  // cdf_t
+        }
+        if (t == 255 || nt >= end) break;
+        prev = cnt;
+        beg = nt;
+        t++;
+        nt = t < 255 ? uint32_t(colp[(t + 1) * kRowU]) : kM;
       }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; u++) {
-      const int e = e0 + u * int(blockDim.x);
-      if (e < n) {
-        const uint32_t p = e % kRowU, b = e / kRowU, slot0 = base + width * b;
-        const uint16_t *colp = cdfc + p;
-        const uint32_t sa = densest_pair<kRowU>(colp, s[u], slot0, width);
-        emit(b, p, sa, sa < 255 ? uint32_t(colp[(sa + 1) * kRowU]) : kM, slot0);
+      emit(b, p, sa, nxt, slot0);
+      // the next bucket's first symbol: t, or past the symbols ending at `end`
+      s = t;
+      cs1 = nt;
+      while (s < 255 && cs1 <= end) {
+        s++;
+        cs1 = s < 255 ? uint32_t(colp[(s + 1) * kRowU]) : kM;
       }
+      slot0 = end;
     }
   }
 }
@@ -668,18 +681,19 @@ __device__ __forceinline__ void build_buckets(const uint16_t *cdfc, int nb, uint
 // last offset of sa's range in the bucket - bias).  For 16-slot buckets bias
 // is the bucket's offset in its 256-slot bucket (16 (b mod 16)), so that the
 // carry out of (x & 255) + entry is the same test as for the main table.
-// Buckets below flag_lo or from flag_hi get 0xFFFF instead.
+// Buckets below flag_lo or from flag_hi get 0xFFFF instead, without a search
+// (a tail bucket of 256 slots can hold hundreds of one-slot symbols).
 __device__ __forceinline__ void build_pairs(uint16_t *lut, const uint16_t *cdfc, int nb, uint32_t width,
                                             uint32_t base, int flag_lo, int flag_hi) {
-  build_buckets(cdfc, nb, width, base, [&](uint32_t b, uint32_t p, uint32_t sa, uint32_t nxt, uint32_t slot0) {
-    uint16_t v = 0xFFFFu;
-    if (int(b) >= flag_lo && int(b) < flag_hi) {
-      const uint32_t bnd = min(nxt - slot0, width) - 1;  // last offset of sa in the bucket
-      const uint32_t bias = width < 256 ? width * (b & (256 / width - 1)) : 0u;
-      v = uint16_t((sa << 8) | (255 - bnd - bias));
-    }
-    lut[b * 128 + p] = v;
-  });
+  for (int e = threadIdx.x; e < nb * 128; e += blockDim.x)
+    if (e / 128 < flag_lo || e / 128 >= flag_hi) lut[e] = 0xFFFFu;
+  build_buckets(cdfc, flag_hi - flag_lo, width, base + width * uint32_t(flag_lo),
+                [&](uint32_t b, uint32_t p, uint32_t sa, uint32_t nxt, uint32_t slot0) {
+                  const uint32_t bb = b + uint32_t(flag_lo);           // the bucket in the table
+                  const uint32_t bnd = min(nxt - slot0, width) - 1;  // last offset of sa in the bucket
+                  const uint32_t bias = width < 256 ? width * (bb & (256 / width - 1)) : 0u;
+                  lut[bb * 128 + p] = uint16_t((sa << 8) | (255 - bnd - bias));
+                });
 }
 
 // Slow lane J (a slot outside the pair its bucket entry names, or the
@@ -705,20 +719,29 @@ __device__ __forceinline__ void slow128(const uint8_t *sm, uint32_t i4, uint32_t
 
 // cmin, cmax: the CTA decodes its level only if the level holds that many
 // chunks in the range (the launches for the other counts take the rest).
+// Grid rows from split0 on come in pairs: the two CTAs of a pair decode the
+// even and the odd entries of the same head's chunk list.
 template <bool PAGED, bool MID>
 __global__ void __launch_bounds__(MID ? kMidTeams * 32 : kTeams128Max * 32, MID ? 2 : 1)
 k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restrict__ buf,
-         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi, int cmin, int cmax) {
+         uint16_t *__restrict__ kv, uint8_t *ws, PagedOut po, int si_lo, int si_hi, int cmin, int cmax,
+         int split0) {
   constexpr int T = 32;
   extern __shared__ __align__(16) uint8_t smb[];
   __shared__ int s_bad;
   uint16_t *cdfc = reinterpret_cast<uint16_t *>(smb + cdf_off<MID>());
 
-  const int lv = blockIdx.x, si = blockIdx.y;
+  const int lv = blockIdx.x;
+  int si = blockIdx.y, part = 0, nparts = 1;
+  if (si >= split0) {
+    si = split0 + (int(blockIdx.y) - split0) / 2;
+    part = (int(blockIdx.y) - split0) & 1;
+    nparts = 2;
+  }
   if (si < si_lo || si >= si_hi) return;  // outside the requested layers
   const int cnt = reinterpret_cast<const int32_t *>(ws + 64)[lv];
   const int nteams = blockDim.x >> 5, first = int(blockIdx.z) * nteams;  // this CTA's entries of the list
-  if (cnt < cmin || cnt > cmax || first >= cnt) return;
+  if (cnt < cmin || cnt > cmax || part + nparts * first >= cnt) return;
   const int32_t *list = reinterpret_cast<const int32_t *>(ws + 256) + lv * lo.n_chunks;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws);
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
@@ -758,7 +781,7 @@ k_dec128(Layout lo, const uint8_t *__restrict__ tables, const uint8_t *__restric
   const float step[4] = {st4.x, st4.y, st4.z, st4.w};
   uint16_t *ring = reinterpret_cast<uint16_t *>(smb + ring_off<MID>()) + team * kRingStride;
 
-  for (int idx = first + team; idx < cnt; idx += nteams * int(gridDim.z)) {
+  for (int idx = part + nparts * (first + team); idx < cnt; idx += nparts * nteams * int(gridDim.z)) {
     const int k = list[idx];
     const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k), nd = chunk_nd(lo, k);
     const uint64_t base = ld_u64(buf + 64 + 8 * uint64_t(k));
@@ -1332,9 +1355,26 @@ cudaError_t launch_decode_128(const Layout &lo, const uint8_t *tables, const uin
   const size_t smem = kRingOff + size_t(teams) * kRingStride * 2;
   cudaError_t e = cudaFuncSetAttribute(k_dec128<PAGED, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, l1 * 2 * lo.H);  // CTAs below layer l0 return at once
+  // The last wave: when the CTAs past the last full wave of the GPU could be
+  // doubled and still run side by side, their heads take two CTAs each, so
+  // that the wave takes about half a CTA's time instead of a whole one.  (Each
+  // level is counted as live; the CTAs of a level in another band return at
+  // once, and the split then only shifts where the waves fall.)
+  const int rows = l1 * 2 * lo.H, live = (l1 - l0) * 2 * lo.H * lo.n_levels;
+  int split = 0, dev = 0, sms = 0, per_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dec128<PAGED, false>, teams * 32, smem);
+  if (e != cudaSuccess) return e;
+  const int wave = sms * per_sm, rest = wave > 0 ? live % wave : 0;
+  if (rest > 0 && chunks >= 2) {
+    const int r = min((rest + lo.n_levels - 1) / lo.n_levels, l1 - l0 > 0 ? (l1 - l0) * 2 * lo.H : 0);
+    if (2 * r * lo.n_levels <= wave) split = r;
+  }
+  dim3 grid(lo.n_levels, rows + split);  // CTAs below layer l0 return at once
   k_dec128<PAGED, false><<<grid, teams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H, l1 * 2 * lo.H,
-                                                         cmin, cmax);
+                                                         cmin, cmax, rows - split);
   return cudaGetLastError();
 }
 
@@ -1353,7 +1393,7 @@ cudaError_t launch_decode_mid(const Layout &lo, const uint8_t *tables, const uin
   if (e != cudaSuccess) return e;
   dim3 grid(lo.n_levels, l1 * 2 * lo.H, (min(chunks, cmax) + kMidTeams - 1) / kMidTeams);
   k_dec128<PAGED, true><<<grid, kMidTeams * 32, smem, st>>>(lo, tables, buf, kv, ws, po, l0 * 2 * lo.H,
-                                                             l1 * 2 * lo.H, cmin, cmax);
+                                                             l1 * 2 * lo.H, cmin, cmax, int(grid.y));
   return cudaGetLastError();
 }
 
