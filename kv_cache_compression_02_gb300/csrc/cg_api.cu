@@ -122,9 +122,11 @@ cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void
   if (e == cudaSuccess && lo.tb_cdf > lo.tb_recip + 4 * nc)
     e = cudaMemsetAsync(tb + lo.tb_recip + 4 * nc, 0, lo.tb_cdf - lo.tb_recip - 4 * nc, st);
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + w.status);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + w.moments, 0, w.bytes - w.moments, st);
   if (e == cudaSuccess)
     e = launch_stats(lo, static_cast<const uint16_t *>(kv_dev), tb,
-                     reinterpret_cast<const float *>(ws + w.mult), bases, status, st);
+                     reinterpret_cast<const float *>(ws + w.mult), bases, status,
+                     reinterpret_cast<uint64_t *>(ws + w.moments), reinterpret_cast<uint32_t *>(ws + w.done), st);
   float2 *scale = reinterpret_cast<float2 *>(ws + w.scale);
   if (e == cudaSuccess)
     e = launch_anchor_scales(lo, static_cast<const uint16_t *>(kv_dev), scale, nullptr, status, st);
@@ -153,12 +155,12 @@ cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *ta
   int32_t *count = reinterpret_cast<int32_t *>(meta.data());
   int32_t *list = count + kMaxLevels;
   uint8_t *lv8 = meta.data() + 4 * kMaxLevels * (1 + nk);
-  int teams = 0;
+  int teams = 0, live_levels = 0;
   for (size_t k = 0; k < nk; k++) {
     const int lv = chunk_level_host[k];
     if (lv >= lo.n_levels) return CG_ERR_INVALID_ARG;
     list[lv * nk + count[lv]] = int32_t(k);
-    count[lv]++;
+    if (count[lv]++ == 0) live_levels++;
     if (count[lv] > teams) teams = count[lv];
     lv8[k] = uint8_t(lv);
   }
@@ -169,7 +171,7 @@ cg_status cg_encode(const cg_dims *dims, const cg_params *params, const void *ta
   if (e == cudaSuccess) e = cudaMemcpyAsync(ws + w.levels, meta.data(), meta.size(), cudaMemcpyHostToDevice, st);
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + w.status);
   if (e == cudaSuccess) e = launch_anchor_scales(lo, kv, nullptr, ws + w.chunks, status, st);
-  if (e == cudaSuccess) e = launch_encode(lo, w, static_cast<const uint8_t *>(tables_dev), kv, ws, teams, st);
+  if (e == cudaSuccess) e = launch_encode(lo, w, static_cast<const uint8_t *>(tables_dev), kv, ws, teams, live_levels, st);
   if (e == cudaSuccess)
     e = launch_scan_compact(lo, w, ws, static_cast<uint8_t *>(out_dev), out_capacity, out_bytes_dev, st);
   return cuda_status(e);

@@ -268,16 +268,25 @@ __device__ __forceinline__ uint32_t suffix_step(uint32_t v) {
   return v;
 }
 
+// Grid rows from split0 on come in pairs: the two CTAs of a pair code the
+// even and the odd entries of the same head's chunk list.
 __global__ void __launch_bounds__(kEncTeams128 * 32, 1)
-k_enc128(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv, uint8_t *ws) {
+k_enc128(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t *__restrict__ kv, uint8_t *ws,
+         int split0) {
   constexpr int T = 32;
   extern __shared__ __align__(16) uint32_t etab[];  // [256][4][32] : cdf | f << 16, then the word rings
-  const int lv = blockIdx.x, si = blockIdx.y;
+  const int lv = blockIdx.x;
+  int si = blockIdx.y, part = 0, nparts = 1;
+  if (si >= split0) {
+    si = split0 + (int(blockIdx.y) - split0) / 2;
+    part = (int(blockIdx.y) - split0) & 1;
+    nparts = 2;
+  }
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
   const int32_t *counts = reinterpret_cast<const int32_t *>(ws + w.levels);
   const int32_t *lists = counts + kMaxLevels;
   const int cnt = counts[lv];
-  if (cnt == 0) return;
+  if (cnt <= part) return;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + w.status);
 
   const uint16_t *cdf = reinterpret_cast<const uint16_t *>(tables + lo.tb_cdf) +
@@ -299,7 +308,7 @@ k_enc128(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
   const float rc[4] = {rc4.x, rc4.y, rc4.z, rc4.w};
   const int R = lo.R;
 
-  for (int idx = team; idx < cnt; idx += nteams) {
+  for (int idx = part + nparts * team; idx < cnt; idx += nparts * nteams) {
     const int k = lists[lv * lo.n_chunks + idx];
     const int ng = chunk_ng(lo, k), ntok = chunk_ntok(lo, k);
     const int64_t t0 = int64_t(k) * lo.C;
@@ -422,14 +431,26 @@ k_enc128(Layout lo, EncWs w, const uint8_t *__restrict__ tables, const uint16_t 
   }
 }
 
+// The last wave, as for the decoder: when the CTAs past the last full wave
+// of the GPU, doubled, still run side by side, their heads take two CTAs each.
 cudaError_t launch_encode_128(const Layout &lo, const EncWs &w, const uint8_t *tables, const uint16_t *kv,
-                              uint8_t *ws, int teams, cudaStream_t st) {
+                              uint8_t *ws, int teams, int live_levels, cudaStream_t st) {
   if (teams > kEncTeams128) teams = kEncTeams128;
   const size_t smem = size_t(256) * 128 * 4 + size_t(teams) * kWordRing * 2;
   cudaError_t e = cudaFuncSetAttribute(k_enc128, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_enc128, teams * 32, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, lo.nstr);
-  k_enc128<<<grid, teams * 32, smem, st>>>(lo, w, tables, kv, ws);
+  const int wave = sms * per_sm, live = lo.nstr * live_levels, rest = wave > 0 ? live % wave : 0;
+  int split = 0;
+  if (rest > 0 && teams >= 2) {
+    const int r = min((rest + live_levels - 1) / live_levels, lo.nstr);
+    if (2 * r * live_levels <= wave) split = r;
+  }
+  dim3 grid(lo.n_levels, lo.nstr + split);
+  k_enc128<<<grid, teams * 32, smem, st>>>(lo, w, tables, kv, ws, lo.nstr - split);
   return cudaGetLastError();
 }
 
@@ -652,14 +673,14 @@ cudaError_t launch_encode_t(const Layout &lo, const EncWs &w, const uint8_t *tab
 }  // namespace
 
 cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,
-                          const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st) {
+                          const uint16_t *kv, uint8_t *ws, int teams, int live_levels, cudaStream_t st) {
   if (teams < 1) return cudaSuccess;
   switch (lo.d / kLpt) {
     case 2: return launch_encode_t<2>(lo, w, tables, kv, ws, teams, st);
     case 4: return launch_encode_t<4>(lo, w, tables, kv, ws, teams, st);
     case 8: return launch_encode_t<8>(lo, w, tables, kv, ws, teams, st);
     case 16: return launch_encode_t<16>(lo, w, tables, kv, ws, teams, st);
-    case 32: return launch_encode_128(lo, w, tables, kv, ws, teams, st);
+    case 32: return launch_encode_128(lo, w, tables, kv, ws, teams, live_levels, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -62,6 +62,10 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 // Each of the three partial sums takes terms below 2^42, so 2^18 tokens
 // per thread (S <= 2^22) keep it below 2^60.  Integer sums are
 // order-free, so the reduction order does not matter for the result.
+// A head's tiles may be shared by `parts` CTAs (so that the last wave of
+// CTAs is not left to a few SMs): each adds its sums to the head's moments
+// with 64-bit atomics (sum X^2 as a 128-bit value, the carry out of the low
+// word added to the high word), and the last to finish computes sigma.
 constexpr int kStatsThreads = 512;
 
 struct Moments {
@@ -107,16 +111,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
 
 __global__ void __launch_bounds__(kStatsThreads, 2)
 k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables,
-        const float *__restrict__ mult, Bases bases, uint32_t *status) {
+        const float *__restrict__ mult, Bases bases, uint32_t *status, unsigned long long *moments,
+        uint32_t *done, int parts) {
   extern __shared__ __align__(128) unsigned char smem[];  // kStatsStages tiles, then the reduction
   __shared__ __align__(8) uint64_t bars[kStatsStages];
   __shared__ uint4 ptab[64];  // per sign and exponent field: (+-2^max(e-1, 0), 2^max(e-1, 0), e ? 1024 : 0)
-  __shared__ int s_timeout;
+  __shared__ int s_timeout, s_last;
   if (threadIdx.x < 64) {
     const uint32_t e = threadIdx.x & 31u, p = e ? 1u << (e - 1) : 1u;
     ptab[threadIdx.x] = make_uint4(threadIdx.x & 32u ? uint32_t(-int32_t(p)) : p, p, e ? 1024u : 0u, 0u);
   }
-  const int si = blockIdx.x;
+  const int si = int(blockIdx.x) / parts, part = int(blockIdx.x) % parts;
   const int tpr = lo.d / 4;                 // threads per token row
   const int rows = kStatsThreads / tpr;     // token rows summed side by side
   const int col = threadIdx.x % tpr, row = threadIdx.x / tpr;
@@ -124,9 +129,10 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   const uint8_t *head = reinterpret_cast<const uint8_t *>(kv + uint64_t(si) * lo.S * lo.d);
   const uint64_t head_bytes = uint64_t(lo.S) * row_bytes;  // a multiple of 16
   const uint64_t ntiles = (head_bytes + kStatsTile - 1) / kStatsTile;
+  const uint64_t t0 = ntiles * uint64_t(part) / uint64_t(parts), t1 = ntiles * uint64_t(part + 1) / uint64_t(parts);
 
-  auto issue = [&](uint64_t t) {  // tile t into stage t % kStatsStages
-    const uint32_t st = uint32_t(t % kStatsStages);
+  auto issue = [&](uint64_t t) {  // tile t into stage (t - t0) % kStatsStages
+    const uint32_t st = uint32_t((t - t0) % kStatsStages);
     const uint64_t left = head_bytes - t * kStatsTile;
     const uint32_t bytes = uint32_t(left < kStatsTile ? left : kStatsTile);
     const uint32_t bar = smem_addr(&bars[st]);
@@ -142,7 +148,7 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     for (uint32_t st = 0; st < kStatsStages; st++)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[st])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (uint64_t t = 0; t < ntiles && t < kStatsStages; t++) issue(t);
+    for (uint64_t t = t0; t < t1 && t < t0 + kStatsStages; t++) issue(t);
   }
   __syncthreads();
 
@@ -150,10 +156,10 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
 #pragma unroll
   for (int i = 0; i < 4; i++) mo[i] = Moments{0, 0, 0, 0};
   uint32_t bad = 0;  // bit 15 of a half: an all-ones exponent (Inf or NaN) was seen
-  uint64_t t = 0;
-  for (; t < ntiles; t++) {
-    const uint32_t st = uint32_t(t % kStatsStages);
-    if (!mbar_wait(smem_addr(&bars[st]), uint32_t(t / kStatsStages) & 1u)) s_timeout = 1;
+  uint64_t t = t0;
+  for (; t < t1; t++) {
+    const uint32_t st = uint32_t((t - t0) % kStatsStages);
+    if (!mbar_wait(smem_addr(&bars[st]), uint32_t((t - t0) / kStatsStages) & 1u)) s_timeout = 1;
     __syncthreads();  // every thread knows whether the tile landed
     if (s_timeout) break;
     const uint8_t *tile = smem + st * kStatsTile;
@@ -167,7 +173,7 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
       for (int i = 0; i < 4; i++) acc_moments(hw[i], ptab, mo[i]);  // a non-finite value only spoils a flagged result
     }
     __syncthreads();  // the stage has been read: it can take the next tile
-    if (threadIdx.x == 0 && t + kStatsStages < ntiles) issue(t + kStatsStages);
+    if (threadIdx.x == 0 && t + kStatsStages < t1) issue(t + kStatsStages);
   }
   // A copy that has not landed after 2^22 try_wait rounds: every tile is an
   // in-bounds, 16-byte aligned read of the caller's kv, which completes
@@ -180,8 +186,8 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
   if (s_timeout) {
     if (threadIdx.x == 0) {
       atomicOr(status, kStTimeout);
-      for (uint64_t u = t; u < ntiles && u < t + kStatsStages; u++)
-        mbar_wait(smem_addr(&bars[u % kStatsStages]), uint32_t(u / kStatsStages) & 1u);
+      for (uint64_t u = t; u < t1 && u < t + kStatsStages; u++)
+        mbar_wait(smem_addr(&bars[(u - t0) % kStatsStages]), uint32_t((u - t0) / kStatsStages) & 1u);
     }
     return;
   }
@@ -200,15 +206,38 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     sB2[c] = mo[i].B2;
   }
   __syncthreads();
+  __int128 Ts = 0;
+  unsigned __int128 Qs = 0;
   if (threadIdx.x < lo.d) {
     const int c = threadIdx.x;
-    __int128 Ts = 0;
-    unsigned __int128 Qs = 0;
     for (int r = 0; r < rows; r++) {
       Ts += sT[r * lo.d + c];
       Qs += ((unsigned __int128)sA2[r * lo.d + c] << 42) + ((unsigned __int128)sAB[r * lo.d + c] << 21) +
             (unsigned __int128)sB2[r * lo.d + c];
     }
+  }
+  if (parts > 1) {  // add to the head's moments; the last CTA of the head goes on with their totals
+    unsigned long long *m = moments + (uint64_t(si) * lo.d + threadIdx.x) * 4;
+    if (threadIdx.x < lo.d) {
+      atomicAdd(&m[0], (unsigned long long)(int64_t)Ts);  // |sum X| < 2^62: two's complement
+      const unsigned long long ql = (unsigned long long)Qs, qh = (unsigned long long)(Qs >> 64);
+      const unsigned long long old = atomicAdd(&m[1], ql);
+      const unsigned long long carry = (old + ql < old) ? 1ull : 0ull;
+      if (qh + carry) atomicAdd(&m[2], qh + carry);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&done[si], 1u) == uint32_t(parts - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x < lo.d) {
+      Ts = (int64_t)atomicAdd(&m[0], 0ull);
+      Qs = ((unsigned __int128)atomicAdd(&m[2], 0ull) << 64) | atomicAdd(&m[1], 0ull);
+    }
+  }
+  if (threadIdx.x < lo.d) {
+    const int c = threadIdx.x;
     unsigned __int128 aT = (unsigned __int128)(Ts < 0 ? -Ts : Ts);
     unsigned __int128 num = (unsigned __int128)(uint64_t)lo.S * Qs - aT * aT;
     double var = __ddiv_rn(u128_to_double_rn(num),
@@ -228,7 +257,7 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
       recipv[ix] = __fdiv_rn(1.0f, st);
     }
   }
-  if (si == 0 && threadIdx.x == 0) {  // tables header
+  if (si == 0 && threadIdx.x == 0) {  // tables header (by the one CTA of head 0 that gets here)
     uint32_t *hd = reinterpret_cast<uint32_t *>(tables);
     hd[0] = 0x42544743u;  // "CGTB"
     hd[1] = 1;
@@ -465,13 +494,37 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
 
 }  // namespace
 
+// parts per head: the number (1 to 8, at least a tile each) with the least
+// estimated time, in tiles: ceil(heads * parts / wave) waves of CTAs, each
+// ceil(tiles / parts) tiles plus about three tiles' worth for the copies'
+// start and the reduction at the end (a CTA's fixed cost, measured on the
+// 70B and 7B workloads: 64-tile heads gain nothing from parts).
 cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
-                         Bases bases, uint32_t *status, cudaStream_t st) {
+                         Bases bases, uint32_t *status, uint64_t *moments, uint32_t *done, cudaStream_t st) {
   const int rows = kStatsThreads / (lo.d / 4);
   const size_t smem = std::max(size_t(kStatsStages) * kStatsTile, size_t(rows) * lo.d * 32);
   cudaError_t e = cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_stats, kStatsThreads, smem);
   if (e != cudaSuccess) return e;
-  k_stats<<<lo.nstr, kStatsThreads, smem, st>>>(lo, kv, tables, mult, bases, status);
+  const int64_t wave = int64_t(sms) * per_sm;
+  const uint64_t ntiles = (uint64_t(lo.S) * 2 * lo.d + kStatsTile - 1) / kStatsTile;
+  int parts = 1;
+  if (wave > 0) {
+    uint64_t best = 0;
+    for (int p = 1; p <= 8 && uint64_t(p) <= ntiles; p++) {
+      const uint64_t waves = uint64_t((int64_t(lo.nstr) * p + wave - 1) / wave);
+      const uint64_t cost = waves * ((ntiles + p - 1) / p + 3);
+      if (p == 1 || cost < best) {
+        best = cost;
+        parts = p;
+      }
+    }
+  }
+  k_stats<<<unsigned(lo.nstr) * unsigned(parts), kStatsThreads, smem, st>>>(
+      lo, kv, tables, mult, bases, status, reinterpret_cast<unsigned long long *>(moments), done, parts);
   return cudaGetLastError();
 }
 

@@ -13,16 +13,19 @@ struct Bases {
 };
 
 // cg_fit.cu
+// moments, done: zeroed workspace ([nstr][d][4] u64 and [nstr] u32) where the
+// CTAs that share a head add up their sums
 cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, const float *mult,
-                         Bases bases, uint32_t *status, cudaStream_t st);
+                         Bases bases, uint32_t *status, uint64_t *moments, uint32_t *done, cudaStream_t st);
 cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *scale_out,
                                  uint8_t *chunk_scratch, uint32_t *status, cudaStream_t st);
 cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
                         uint8_t *tables, double *ent_bits, uint32_t *ent_esc, cudaStream_t st);
 
 // cg_encode.cu
+// teams: the most chunks a level holds; live_levels: the levels holding any
 cudaError_t launch_encode(const Layout &lo, const EncWs &w, const uint8_t *tables,
-                          const uint16_t *kv, uint8_t *ws, int teams, cudaStream_t st);
+                          const uint16_t *kv, uint8_t *ws, int teams, int live_levels, cudaStream_t st);
 cudaError_t launch_scan_compact(const Layout &lo, const EncWs &w, uint8_t *ws, uint8_t *out,
                                 uint64_t cap, uint64_t *out_bytes, cudaStream_t st);
 

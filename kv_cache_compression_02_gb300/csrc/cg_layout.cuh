@@ -110,7 +110,7 @@ __host__ __device__ inline uint64_t words_per_symbol(const Layout &lo) { return 
 // ---- workspaces ----------------------------------------------------------
 // Every workspace starts with a 256-byte status block.
 struct FitWs {
-  uint64_t status, mult, scale, ent_bits, ent_esc, bytes;  // offsets
+  uint64_t status, mult, scale, ent_bits, ent_esc, moments, done, bytes;  // offsets
 };
 inline FitWs fit_ws(const Layout &lo) {
   FitWs w;
@@ -120,7 +120,9 @@ inline FitWs fit_ws(const Layout &lo) {
   w.scale = pad256(w.mult + 8 * uint64_t(lo.L));                  // f32x2 [nk][nstr*d]
   w.ent_bits = pad256(w.scale + 8 * uint64_t(lo.n_chunks) * lo.nstr * lo.d);  // f64 [tables]
   w.ent_esc = pad256(w.ent_bits + 8 * nc);                        // u32 [tables]
-  w.bytes = pad256(w.ent_esc + 4 * nc);
+  w.moments = pad256(w.ent_esc + 4 * nc);                         // u64 [nstr][d][4]: sum X, sum X^2 (lo, hi)
+  w.done = pad256(w.moments + 32 * uint64_t(lo.nstr) * lo.d);     // u32 [nstr]: parts of a head summed
+  w.bytes = pad256(w.done + 4 * uint64_t(lo.nstr));
   return w;
 }
 
