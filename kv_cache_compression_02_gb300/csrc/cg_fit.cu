@@ -58,7 +58,7 @@ __device__ __forceinline__ double u128_to_double_rn(unsigned __int128 v) {
 // 32x32->64 multiply-adds, which run on the FMA pipe beside the integer ALU:
 //   sum X    += M * (+-2^E)                      (signed, 64-bit)
 //   X = a 2^21 + b (a < 2^20, b < 2^21):
-//   sum X^2  = 2^42 sum a^2 + 2^21 sum 2ab + sum b^2
+//   sum X^2  = 2^42 sum a^2 + 2^22 sum ab + sum b^2
 // Each of the three partial sums takes terms below 2^42, so 2^18 tokens
 // per thread (S <= 2^22) keep it below 2^60.  Integer sums are
 // order-free, so the reduction order does not matter for the result.
@@ -73,15 +73,19 @@ struct Moments {
   uint64_t A2, AB, B2;
 };
 
+// Each sum is one 32x32->64 multiply-add with its 64-bit accumulator as the
+// addend; AB sums a*b, and the reduction doubles it (2^22 instead of 2^21).
 __device__ __forceinline__ void acc_moments(uint32_t h, const uint4 *ptab, Moments &m) {
   const uint4 pe = ptab[h >> 10];  // (+-2^E with h's sign, 2^E, the implicit bit of M)
   const uint32_t M = (h & 1023u) | pe.z;
-  const uint64_t X = uint64_t(M) * pe.y;
-  m.T += int64_t(int32_t(M)) * int32_t(pe.x);
-  const uint32_t a = uint32_t(X >> 21), b = uint32_t(X) & 0x1FFFFFu;
-  m.A2 += uint64_t(a) * a;
-  m.AB += uint64_t(a) * (2u * b);
-  m.B2 += uint64_t(b) * b;
+  uint64_t X;
+  asm("mul.wide.u32 %0, %1, %2;" : "=l"(X) : "r"(M), "r"(pe.y));
+  asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(m.T) : "r"(M), "r"(pe.x));
+  const uint32_t xl = uint32_t(X), xh = uint32_t(X >> 32);
+  const uint32_t a = __funnelshift_r(xl, xh, 21), b = xl & 0x1FFFFFu;  // X = a 2^21 + b
+  asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(m.A2) : "r"(a));
+  asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(m.AB) : "r"(a), "r"(b));
+  asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(m.B2) : "r"(b));
 }
 
 // The head's rows stream through shared memory in 16 KB tiles, four in
@@ -212,7 +216,7 @@ k_stats(Layout lo, const uint16_t *__restrict__ kv, uint8_t *__restrict__ tables
     const int c = threadIdx.x;
     for (int r = 0; r < rows; r++) {
       Ts += sT[r * lo.d + c];
-      Qs += ((unsigned __int128)sA2[r * lo.d + c] << 42) + ((unsigned __int128)sAB[r * lo.d + c] << 21) +
+      Qs += ((unsigned __int128)sA2[r * lo.d + c] << 42) + ((unsigned __int128)sAB[r * lo.d + c] << 22) +
             (unsigned __int128)sB2[r * lo.d + c];
     }
   }
