@@ -264,9 +264,8 @@ cg_status cg_decode_paged(const cg_dims *dims, const cg_params *params, const vo
  *   status_ws: if not NULL, receives the device address of that array;
  *              pass it to cg_read_status() after synchronising.
  * The first call on each device looks the array's address up and keeps it
- * for the life of the process (make that first call before any stream
- * capture); after cudaDeviceReset the kept address is stale, so do not call
- * this entry point again in that process.  All calls share the array and it
+ * for the life of the process; after cudaDeviceReset the kept address is
+ * stale, so do not call this entry point again in that process.  All calls share the array and it
  * keeps the last call's contents: each call clears the status first, and
  * calls that overlap on the GPU race on it, so serialise them.  It calls no
  * allocating routine. */
