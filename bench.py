@@ -521,13 +521,18 @@ def main():
         link[name] = nb_ / (statistics.mean(ts) * 1e-3) / 1e9
 
     # chunk-group streaming: group g's container bytes are copied from pinned
-    # host memory on one stream, and the group decodes on another as soon as
-    # they have landed, while group g + 1 is being copied; against the copy
-    # alone and the one-shot decode from device memory
+    # host memory on one stream, and the group decodes as soon as they have
+    # landed, while group g + 1 is being copied; the groups' decodes alternate
+    # between two streams, each with its own workspace, so that a group's
+    # launches can fill the SMs the previous group's last wave leaves idle
+    # (the groups write disjoint tokens); against the copy alone and the
+    # one-shot decode from device memory
     streamed = None
     if args.stream_groups:
         G = args.stream_groups
         copy_s, dec_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        dec_s2 = torch.cuda.Stream(device=dev)
+        ws_dec2 = cg.empty_u8(cg.cg_workspace_bytes(cfg, cg.CG_OP_DECODE))
         win = [(lo_, lo_ + (1 << 22)) for lo_ in (0, kv.numel() // 2, kv.numel() - (1 << 22))]
         ref = [kv_out[a_:b_].clone() for a_, b_ in win]  # kv_out holds the serial end-to-end decode
 
@@ -541,15 +546,19 @@ def main():
             return a.elapsed_time(b)
 
         def stream_groups():
-            for g0 in range(0, w.n_chunks, G):
+            for gi, g0 in enumerate(range(0, w.n_chunks, G)):
                 g1 = min(g0 + G, w.n_chunks)
                 lo_b = 0 if g0 == 0 else offs[g0]  # the first group carries the header and chunk index
                 with torch.cuda.stream(copy_s):
                     cont_dev[lo_b:offs[g1]].copy_(cont_host[lo_b:offs[g1]], non_blocking=True)
                 arrived = torch.cuda.Event()
                 arrived.record(copy_s)
-                dec_s.wait_event(arrived)
-                cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, g0, g1, kv_out, ws_dec, dec_s), "cg_decode")
+                ds, wsd = (dec_s, ws_dec) if gi % 2 == 0 else (dec_s2, ws_dec2)
+                ds.wait_event(arrived)
+                cg.check(cg.cg_decode(cfg, tables, cont_dev, nbytes, g0, g1, kv_out, wsd, ds), "cg_decode")
+            done2 = torch.cuda.Event()
+            done2.record(dec_s2)
+            dec_s.wait_event(done2)  # the end event, on dec_s, follows both decode streams
 
         def copy_alone():
             with torch.cuda.stream(copy_s):
@@ -561,6 +570,7 @@ def main():
         kv_out.zero_()
         t_stream = [timed(stream_groups, copy_s, dec_s) for _ in range(3)]
         cg.check(cg.cg_read_status(ws_dec), "decode (streamed)")
+        cg.check(cg.cg_read_status(ws_dec2), "decode (streamed)")
         for (a_, b_), r_ in zip(win, ref):
             if not torch.equal(kv_out[a_:b_], r_):
                 raise RuntimeError("streamed decode differs from the one-shot decode")
@@ -570,8 +580,8 @@ def main():
         streamed = {"groups_of_chunks": G, "ms": t_s, "copy_ms": t_copy, "decode_ms": t_dec,
                     "overlap_efficiency": max(t_copy, t_dec) / t_s, "fp16_gbs": w.fp16_bytes / (t_s * 1e-3) / 1e9,
                     "what": "container copied group by group from pinned host memory on one stream, each group "
-                            "decoded on another once its bytes have landed; efficiency = max(copy alone, one-shot "
-                            "decode) / streamed"}
+                            "decoded once its bytes have landed, on two streams in turn (a workspace each); "
+                            "efficiency = max(copy alone, one-shot decode) / streamed"}
         del ref
 
     # the same decode in layer groups, in execution order: 19 layers (304
