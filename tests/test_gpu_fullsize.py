@@ -7,7 +7,7 @@ block, scales and int8 anchors byte for byte against its own encode with the
 GPU's table rows, the table rows against its own fit, the decoded fp16
 tokens against its own decode of the container's streams, and the chunk
 index and stream offsets against its stream lengths.  Each container is also held to the entropy bound of its
-coded symbols: at most 1% above it (the spec gate of the codec).  The
+coded symbols: at most 1% above it (the codec's compression gate).  The
 long-context mixed-level workload is also decoded chunk group by chunk group
 on a side stream while the next group is copied from pinned host memory, and
 must equal the one-shot decode.
