@@ -132,7 +132,8 @@ cg_status cg_fit_tables(const cg_dims *dims, const cg_params *params, const void
     e = launch_anchor_scales(lo, static_cast<const uint16_t *>(kv_dev), scale, nullptr, status, st);
   if (e == cudaSuccess)
     e = launch_hist(lo, static_cast<const uint16_t *>(kv_dev), scale, tb, reinterpret_cast<double *>(ws + w.ent_bits),
-                    reinterpret_cast<uint32_t *>(ws + w.ent_esc), st);
+                    reinterpret_cast<uint32_t *>(ws + w.ent_esc), reinterpret_cast<uint32_t *>(ws + w.pair_hist),
+                    reinterpret_cast<uint32_t *>(ws + w.pair_done), st);
   return cuda_status(e);
 }
 

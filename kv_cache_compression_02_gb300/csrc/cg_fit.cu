@@ -353,13 +353,27 @@ k_anchor(Layout lo, const uint16_t *__restrict__ kv, float2 *__restrict__ scale_
 // its counts and records, for the entropy bound of a container coded with
 // this level, the bits its symbols carry at their own frequencies,
 // sum_s n_s log2(N / n_s) (log2 in fp32, summed in fp64), and its escapes.
+// Grid rows from split0 on come in pairs (the last wave's heads): the two
+// CTAs of a pair count the first and the second half of the head's groups,
+// add their histograms into the pair's in the workspace, and the one that
+// finishes last normalises the sum (integer counts: exact in any order).
 constexpr int kHistThreads = 1024;
 
 __global__ void __launch_bounds__(kHistThreads)
 k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ scale,
-       uint8_t *__restrict__ tables, double *__restrict__ ent_bits, uint32_t *__restrict__ ent_esc) {
+       uint8_t *__restrict__ tables, double *__restrict__ ent_bits, uint32_t *__restrict__ ent_esc,
+       uint32_t *pair_hist, uint32_t *pair_done, int split0) {
   extern __shared__ __align__(16) uint32_t hist[];  // [d][257]
-  const int lv = blockIdx.x, si = blockIdx.y;
+  __shared__ int s_last;
+  const int lv = blockIdx.x;
+  int si = blockIdx.y, part = 0, nparts = 1, pair = 0;
+  if (si >= split0) {
+    const int j = int(blockIdx.y) - split0;
+    si = split0 + j / 2;
+    part = j & 1;
+    nparts = 2;
+    pair = (j / 2) * int(gridDim.x) + lv;  // below kHistPairsMax (the launcher's bound)
+  }
   const int h = si % lo.H, kvi = (si / lo.H) % 2, l = si / (2 * lo.H);
   for (int i = threadIdx.x; i < lo.d * 257; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -378,9 +392,10 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
   for (int i = 0; i < 4; i++) hrow[i] = hist + (i * tpr + col) * 257;
   const uint2 *head = reinterpret_cast<const uint2 *>(kv + uint64_t(si) * lo.S * lo.d + c0);
   const int64_t n_groups = int64_t(lo.n_chunks - 1) * lo.ng_full + lo.ng_last;
+  const int64_t g_lo = n_groups * part / nparts, g_hi = n_groups * (part + 1) / nparts;
   const uint32_t R = uint32_t(lo.R);
 
-  for (int64_t gi = team; gi < n_groups; gi += teams) {
+  for (int64_t gi = g_lo + team; gi < g_hi; gi += teams) {
     const int k = int(gi / lo.ng_full), g = int(gi % lo.ng_full);
     const int64_t t0 = int64_t(k) * lo.C;
     const int64_t ta = t0 + int64_t(g) * lo.G;
@@ -426,6 +441,19 @@ k_hist(Layout lo, const uint16_t *__restrict__ kv, const float2 *__restrict__ sc
 #undef CG_COUNT_ROW
   }
   __syncthreads();
+  if (nparts > 1) {
+    uint32_t *gh = pair_hist + uint64_t(pair) * lo.d * 257;
+    for (int i = threadIdx.x; i < lo.d * 257; i += blockDim.x)
+      if (hist[i]) atomicAdd(&gh[i], hist[i]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&pair_done[pair], 1u) == 1u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < lo.d * 257; i += blockDim.x) hist[i] = __ldcg(&gh[i]);
+    __syncthreads();
+  }
 
   // normalisation: one warp per channel, 8 symbols per lane
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -539,13 +567,28 @@ cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *s
   return cudaGetLastError();
 }
 
+// The last wave, as for the decoder: when the CTAs past the last full wave,
+// doubled, still run side by side (and the pairs fit the workspace), their
+// (level, head) units take two CTAs each.
 cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
-                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, cudaStream_t st) {
+                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, uint32_t *pair_hist,
+                        uint32_t *pair_done, cudaStream_t st) {
   const size_t smem = size_t(lo.d) * 257 * 4;
   cudaError_t e = cudaFuncSetAttribute(k_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_hist, kHistThreads, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(lo.n_levels, lo.nstr);
-  k_hist<<<grid, kHistThreads, smem, st>>>(lo, kv, scale, tables, ent_bits, ent_esc);
+  const int wave = sms * per_sm, live = lo.nstr * lo.n_levels, rest = wave > 0 ? live % wave : 0;
+  int split = 0;
+  if (rest > 0) {
+    const int r = min((rest + lo.n_levels - 1) / lo.n_levels, lo.nstr);
+    if (2 * r * lo.n_levels <= wave && r * lo.n_levels <= kHistPairsMax) split = r;
+  }
+  dim3 grid(lo.n_levels, lo.nstr + split);
+  k_hist<<<grid, kHistThreads, smem, st>>>(lo, kv, scale, tables, ent_bits, ent_esc, pair_hist, pair_done,
+                                           lo.nstr - split);
   return cudaGetLastError();
 }
 

@@ -19,8 +19,11 @@ cudaError_t launch_stats(const Layout &lo, const uint16_t *kv, uint8_t *tables, 
                          Bases bases, uint32_t *status, uint64_t *moments, uint32_t *done, cudaStream_t st);
 cudaError_t launch_anchor_scales(const Layout &lo, const uint16_t *kv, float2 *scale_out,
                                  uint8_t *chunk_scratch, uint32_t *status, cudaStream_t st);
+// pair_hist, pair_done: zeroed workspace ([kHistPairsMax][d][257] and
+// [kHistPairsMax] u32) where the two CTAs of a shared (level, head) meet
 cudaError_t launch_hist(const Layout &lo, const uint16_t *kv, const float2 *scale,
-                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, cudaStream_t st);
+                        uint8_t *tables, double *ent_bits, uint32_t *ent_esc, uint32_t *pair_hist,
+                        uint32_t *pair_done, cudaStream_t st);
 
 // cg_encode.cu
 // teams: the most chunks a level holds; live_levels: the levels holding any

@@ -109,8 +109,11 @@ __host__ __device__ inline uint64_t words_per_symbol(const Layout &lo) { return 
 
 // ---- workspaces ----------------------------------------------------------
 // Every workspace starts with a 256-byte status block.
+// Histogram pairs: (level, head) pairs of the histogram pass's last wave
+// that two CTAs share, at most this many.
+constexpr int kHistPairsMax = 96;
 struct FitWs {
-  uint64_t status, mult, scale, ent_bits, ent_esc, moments, done, bytes;  // offsets
+  uint64_t status, mult, scale, ent_bits, ent_esc, moments, done, pair_hist, pair_done, bytes;  // offsets
 };
 inline FitWs fit_ws(const Layout &lo) {
   FitWs w;
@@ -122,7 +125,9 @@ inline FitWs fit_ws(const Layout &lo) {
   w.ent_esc = pad256(w.ent_bits + 8 * nc);                        // u32 [tables]
   w.moments = pad256(w.ent_esc + 4 * nc);                         // u64 [nstr][d][4]: sum X, sum X^2 (lo, hi)
   w.done = pad256(w.moments + 32 * uint64_t(lo.nstr) * lo.d);     // u32 [nstr]: parts of a head summed
-  w.bytes = pad256(w.done + 4 * uint64_t(lo.nstr));
+  w.pair_hist = pad256(w.done + 4 * uint64_t(lo.nstr));           // u32 [kHistPairsMax][d][257]
+  w.pair_done = pad256(w.pair_hist + 4 * uint64_t(kHistPairsMax) * lo.d * 257);  // u32 [kHistPairsMax]
+  w.bytes = pad256(w.pair_done + 4 * uint64_t(kHistPairsMax));
   return w;
 }
 
